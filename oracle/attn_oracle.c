@@ -1,0 +1,379 @@
+/*
+ * attn_oracle.c — plain, slow fp64 CPU oracle for scaled-dot-product attention
+ * (forward producing O and the per-row log-sum-exp, and the backward pass).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header, table or helper with the
+ * CUDA path.
+ *
+ * What it follows (page titles as printed; sections as numbered there):
+ *   - "ops(8)：self-attention 的 CUDA 实现及优化 (下) - 深度分析",
+ *       §2.1 "反向传播数学推导" (matrix-product derivative, softmax derivative,
+ *       forward S = QK^T/sqrt(d_k), P = softmax(S), O = PV, and the five-step
+ *       backward chain rule dV, dP, dS, dQ, dK);
+ *       §2.2 "CPU 参考实现" (loop structure of the explicit softmax-Jacobian
+ *       backward, causal visibility t2 <= t, scale applied to dpreatt);
+ *       Appendix A.1-A.3 (the same formulas restated).
+ *   - "深度学习反向传播优化：2-CTA MMA模式与内存访问优化" does not change the
+ *       arithmetic; it is about how a kernel schedules it.
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes of the repository):
+ *   - The scale s multiplies the scores: S = s * Q K^T, with s passed in
+ *     (the pages use s = 1/sqrt(d_k)).  dQ = s * dS K and dK = s * dS^T Q.
+ *   - The softmax statistic that the forward returns is the natural-log
+ *     log-sum-exp of the scaled scores: LSE_i = ln sum_j exp(S_ij).
+ *   - Causal visibility is key j visible to query i iff j <= i (top-left
+ *     aligned); it is only defined here for Tq == Tk.
+ *
+ * Data layout: a "problem" is one (sequence, head) pair.  All matrices are
+ * fp64, row-major, one row per token:
+ *   Q, dO, O, dQ : rows qrow0[p] .. qrow0[p]+Tq[p]-1 of [*, dqk] / [*, dv]
+ *   K, V, dK, dV : rows krow0[p] .. krow0[p]+Tk[p]-1 of [*, dqk] / [*, dv]
+ *   LSE, D       : entries qrow0[p] .. (one per query row)
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/*
+ * ORACLE_PLANT selects a deliberately wrong variant for the mutation tests
+ * (which check that the pins catch plausible mistakes).  It is 0 in every
+ * build that is used as the oracle.
+ *   1: dQ without the scale factor        2: wrong sign of D in dS
+ *   3: causal mask off by one (j < i)     4: dV indexed by the key's own row
+ *   5: LSE returned in log base 2         6: dK takes dS^T K instead of dS^T Q
+ */
+#ifndef ORACLE_PLANT
+#define ORACLE_PLANT 0
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_NOMEM (-2)
+
+static int visible(int causal, int i, int j) {
+  if (ORACLE_PLANT == 3) return causal ? (j < i || (i == 0 && j == 0)) : 1;
+  return causal ? (j <= i) : 1;
+}
+
+/* Number of keys query row i may look at (keys 0 .. n-1). */
+static int n_visible(int causal, int i, int Tk) {
+  if (!causal) return Tk;
+  if (ORACLE_PLANT == 3 && i > 0) return i;
+  return (i + 1 < Tk) ? i + 1 : Tk;
+}
+
+static int check_problem(int causal, int Tq, int Tk) {
+  if (Tq < 0 || Tk <= 0) return ORACLE_ERR_ARG;
+  if (causal && Tq != Tk) return ORACLE_ERR_ARG;
+  return ORACLE_OK;
+}
+
+/*
+ * One query row of the forward, by definition (§2.1 forward, Appendix A.1):
+ *   S_ij = s * sum_c Q_ic K_jc            for visible j
+ *   P_ij = exp(S_ij) / sum_j' exp(S_ij')   (softmax; max subtracted first)
+ *   O_i  = sum_j P_ij V_j
+ *   LSE_i = ln sum_j exp(S_ij)
+ * `P` receives the probabilities of the n visible keys (caller's scratch).
+ */
+static void forward_row(const double *q, const double *K, const double *V,
+                        int n, int dqk, int dv, double scale, double *P,
+                        double *o, double *lse) {
+  double m = -INFINITY;
+  for (int j = 0; j < n; j++) {
+    double s = 0.0;
+    for (int c = 0; c < dqk; c++) s += q[c] * K[(long long)j * dqk + c];
+    s *= scale;
+    P[j] = s;
+    if (s > m) m = s;
+  }
+  double sum = 0.0;
+  for (int j = 0; j < n; j++) {
+    P[j] = exp(P[j] - m);
+    sum += P[j];
+  }
+  for (int j = 0; j < n; j++) P[j] /= sum;
+  if (o) {
+    for (int c = 0; c < dv; c++) o[c] = 0.0;
+    for (int j = 0; j < n; j++)
+      for (int c = 0; c < dv; c++) o[c] += P[j] * V[(long long)j * dv + c];
+  }
+  if (lse) *lse = (ORACLE_PLANT == 5) ? (m + log(sum)) / log(2.0) : m + log(sum);
+}
+
+/* dP_ij = sum_c dO_ic V_jc   (§2.1 backward step 2: dP = dO V^T) */
+static void dp_row(const double *dout, const double *V, int n, int dv,
+                   double *dP) {
+  for (int j = 0; j < n; j++) {
+    double s = 0.0;
+    for (int c = 0; c < dv; c++) s += dout[c] * V[(long long)j * dv + c];
+    dP[j] = s;
+  }
+}
+
+/*
+ * Forward over all problems.  Rows are independent, so the loop runs over
+ * every (problem, query row) pair.  When dO and D are given it also returns
+ * D_i = sum_j P_ij dP_ij (the row sum that the softmax backward subtracts,
+ * §2.1 step 3, written from its definition).
+ */
+int oracle_forward(int nprob, const long long *qrow0, const int *Tq,
+                   const long long *krow0, const int *Tk, int dqk, int dv,
+                   int causal, double scale, const double *Q, const double *K,
+                   const double *V, const double *dO, double *O, double *LSE,
+                   double *D) {
+  if (nprob < 0 || dqk <= 0 || dv <= 0) return ORACLE_ERR_ARG;
+  long long total = 0;
+  int maxTk = 1;
+  for (int p = 0; p < nprob; p++) {
+    if (check_problem(causal, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
+    total += Tq[p];
+    if (Tk[p] > maxTk) maxTk = Tk[p];
+  }
+  /* flattened (problem, row) index */
+  long long *start = (long long *)malloc(sizeof(long long) * (nprob + 1));
+  if (!start) return ORACLE_ERR_NOMEM;
+  start[0] = 0;
+  for (int p = 0; p < nprob; p++) start[p + 1] = start[p] + Tq[p];
+  int err = ORACLE_OK;
+#pragma omp parallel
+  {
+    double *P = (double *)malloc(sizeof(double) * maxTk);
+    double *dP = (double *)malloc(sizeof(double) * maxTk);
+    if (!P || !dP) {
+#pragma omp atomic write
+      err = ORACLE_ERR_NOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 8)
+      for (long long r = 0; r < total; r++) {
+        int lo = 0, hi = nprob - 1; /* problem holding flattened row r */
+        while (lo < hi) {
+          int mid = (lo + hi + 1) / 2;
+          if (start[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        int p = lo;
+        int i = (int)(r - start[p]);
+        long long qi = qrow0[p] + i;
+        const double *Kp = K + krow0[p] * dqk;
+        const double *Vp = V + krow0[p] * dv;
+        int n = n_visible(causal, i, Tk[p]);
+        double lse;
+        forward_row(Q + qi * dqk, Kp, Vp, n, dqk, dv, scale, P,
+                    O ? O + qi * dv : NULL, &lse);
+        if (LSE) LSE[qi] = lse;
+        if (dO && D) {
+          dp_row(dO + qi * dv, Vp, n, dv, dP);
+          double d = 0.0;
+          for (int j = 0; j < n; j++) d += P[j] * dP[j];
+          D[qi] = d;
+        }
+      }
+    }
+    free(P);
+    free(dP);
+  }
+  free(start);
+  return err;
+}
+
+/*
+ * Backward of one problem, row by row, for the query rows listed in `rows`
+ * (all rows when rows == NULL).  For each row i (§2.1 backward, steps 1-5):
+ *   P_i  = softmax(S_i)                      (recomputed from Q, K)
+ *   dV_j += P_ij dO_i                         (step 1: dV = P^T dO)
+ *   dP_ij = dO_i . V_j                        (step 2: dP = dO V^T)
+ *   dS_i  = softmax backward of dP_i          (step 3)
+ *   dQ_i  = s sum_j dS_ij K_j                 (step 4: dQ = dS K / sqrt(d_k))
+ *   dK_j += s dS_ij Q_i                       (step 5: dK = dS^T Q / sqrt(d_k))
+ * Step 3 has two forms:
+ *   mode 0 (row JVP):  dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)
+ *   mode 1 (explicit Jacobian, as in the §2.2 CPU loop and the softmax
+ *           derivative of §2.1 / Appendix A.3):
+ *           J_kj = P_ik (delta_kj - P_ij);  dS_ij = sum_k J_kj dP_ik
+ * dK and dV of the problem are zeroed first and receive the contributions of
+ * the listed rows only; with all rows they are the full gradients.
+ * Optional per-row outputs: O, LSE, D (= sum_j P_ij dP_ij), dQ, and for tiny
+ * cases the full Tq x Tk matrices P and dS of the problem (zero where masked).
+ */
+static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
+                            int causal, double scale, const double *Q,
+                            const double *K, const double *V, const double *dO,
+                            const int *rows, int nrows, double *dQ, double *dK,
+                            double *dV, double *O, double *LSE, double *D,
+                            double *Pfull, double *dSfull) {
+  double *P = (double *)malloc(sizeof(double) * Tk);
+  double *dP = (double *)malloc(sizeof(double) * Tk);
+  double *dS = (double *)malloc(sizeof(double) * Tk);
+  if (!P || !dP || !dS) {
+    free(P); free(dP); free(dS);
+    return ORACLE_ERR_NOMEM;
+  }
+  if (dK) memset(dK, 0, sizeof(double) * (size_t)Tk * dqk);
+  if (dV) memset(dV, 0, sizeof(double) * (size_t)Tk * dv);
+  if (Pfull) memset(Pfull, 0, sizeof(double) * (size_t)Tq * Tk);
+  if (dSfull) memset(dSfull, 0, sizeof(double) * (size_t)Tq * Tk);
+  int count = rows ? nrows : Tq;
+  for (int r = 0; r < count; r++) {
+    int i = rows ? rows[r] : r;
+    if (i < 0 || i >= Tq) continue;
+    int n = n_visible(causal, i, Tk);
+    const double *qi = Q + (long long)i * dqk;
+    const double *doi = dO + (long long)i * dv;
+    double lse;
+    forward_row(qi, K, V, n, dqk, dv, scale, P, O ? O + (long long)i * dv : NULL,
+                &lse);
+    if (LSE) LSE[i] = lse;
+    dp_row(doi, V, n, dv, dP);
+    double rowdot = 0.0;
+    for (int j = 0; j < n; j++) rowdot += P[j] * dP[j];
+    if (D) D[i] = rowdot;
+    if (mode == 0) {
+      for (int j = 0; j < n; j++)
+        dS[j] = P[j] * (dP[j] - (ORACLE_PLANT == 2 ? -rowdot : rowdot));
+    } else {
+      for (int j = 0; j < n; j++) {
+        double acc = 0.0;
+        for (int k = 0; k < n; k++) {
+          double jac = P[k] * ((k == j ? 1.0 : 0.0) - P[j]);
+          acc += jac * dP[k];
+        }
+        dS[j] = acc;
+      }
+    }
+    if (dV)
+      for (int j = 0; j < n; j++)
+        for (int c = 0; c < dv; c++)
+          dV[(long long)j * dv + c] +=
+              P[j] * (ORACLE_PLANT == 4 ? dO[(long long)j * dv + c] : doi[c]);
+    if (dQ) {
+      double *dqi = dQ + (long long)i * dqk;
+      for (int c = 0; c < dqk; c++) dqi[c] = 0.0;
+      for (int j = 0; j < n; j++)
+        for (int c = 0; c < dqk; c++)
+          dqi[c] += (ORACLE_PLANT == 1 ? 1.0 : scale) * dS[j] *
+                    K[(long long)j * dqk + c];
+    }
+    if (dK)
+      for (int j = 0; j < n; j++)
+        for (int c = 0; c < dqk; c++)
+          dK[(long long)j * dqk + c] +=
+              scale * dS[j] * (ORACLE_PLANT == 6 ? K[(long long)i * dqk + c] : qi[c]);
+    if (Pfull)
+      for (int j = 0; j < n; j++) Pfull[(long long)i * Tk + j] = P[j];
+    if (dSfull)
+      for (int j = 0; j < n; j++) dSfull[(long long)i * Tk + j] = dS[j];
+  }
+  free(P); free(dP); free(dS);
+  return ORACLE_OK;
+}
+
+/*
+ * Backward over all problems (parallel over problems; the rows of one problem
+ * run in order because dK and dV accumulate over them).
+ * rows/nrows: optional per-problem row subsets, concatenated; rows == NULL
+ * means every row.  Pfull / dSfull (optional) are concatenated Tq x Tk blocks.
+ */
+int oracle_backward(int mode, int nprob, const long long *qrow0, const int *Tq,
+                    const long long *krow0, const int *Tk, int dqk, int dv,
+                    int causal, double scale, const double *Q, const double *K,
+                    const double *V, const double *dO, const int *rows,
+                    const int *nrows, double *dQ, double *dK, double *dV,
+                    double *O, double *LSE, double *D, double *Pfull,
+                    double *dSfull) {
+  if (nprob < 0 || dqk <= 0 || dv <= 0 || (mode != 0 && mode != 1))
+    return ORACLE_ERR_ARG;
+  for (int p = 0; p < nprob; p++)
+    if (check_problem(causal, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
+  long long *row_start = (long long *)calloc(nprob + 1, sizeof(long long));
+  long long *pt_start = (long long *)calloc(nprob + 1, sizeof(long long));
+  if (!row_start || !pt_start) {
+    free(row_start); free(pt_start);
+    return ORACLE_ERR_NOMEM;
+  }
+  for (int p = 0; p < nprob; p++) {
+    row_start[p + 1] = row_start[p] + (rows ? nrows[p] : 0);
+    pt_start[p + 1] = pt_start[p] + (long long)Tq[p] * Tk[p];
+  }
+  int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int p = 0; p < nprob; p++) {
+    long long q0 = qrow0[p], k0 = krow0[p];
+    int e = backward_problem(
+        mode, Tq[p], Tk[p], dqk, dv, causal, scale, Q + q0 * dqk, K + k0 * dqk,
+        V + k0 * dv, dO + q0 * dv, rows ? rows + row_start[p] : NULL,
+        rows ? nrows[p] : 0, dQ ? dQ + q0 * dqk : NULL,
+        dK ? dK + k0 * dqk : NULL, dV ? dV + k0 * dv : NULL,
+        O ? O + q0 * dv : NULL, LSE ? LSE + q0 : NULL, D ? D + q0 : NULL,
+        Pfull ? Pfull + pt_start[p] : NULL, dSfull ? dSfull + pt_start[p] : NULL);
+    if (e) {
+#pragma omp atomic write
+      err = e;
+    }
+  }
+  free(row_start);
+  free(pt_start);
+  return err;
+}
+
+/*
+ * dK and dV rows for selected keys of one problem, one key at a time, given
+ * the forward statistics LSE_i and D_i of every query row (from
+ * oracle_forward).  For key j (§2.1 steps 1-3 and 5, column form):
+ *   P_ij  = exp(s Q_i.K_j - LSE_i)          for queries i that see key j
+ *   dV_j  = sum_i P_ij dO_i
+ *   dS_ij = P_ij (dO_i.V_j - D_i)
+ *   dK_j  = s sum_i dS_ij Q_i
+ * Parallel over the listed keys.  Outputs are [nkeys][dqk] and [nkeys][dv].
+ */
+int oracle_kv_rows(int Tq, int Tk, int dqk, int dv, int causal, double scale,
+                   const double *Q, const double *K, const double *V,
+                   const double *dO, const double *LSE, const double *D,
+                   const int *keys, int nkeys, double *dK_rows,
+                   double *dV_rows) {
+  if (check_problem(causal, Tq, Tk) || dqk <= 0 || dv <= 0)
+    return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < nkeys; t++) {
+    int j = keys[t];
+    double *dk = dK_rows + (long long)t * dqk;
+    double *dvr = dV_rows + (long long)t * dv;
+    for (int c = 0; c < dqk; c++) dk[c] = 0.0;
+    for (int c = 0; c < dv; c++) dvr[c] = 0.0;
+    if (j < 0 || j >= Tk) continue;
+    const double *kj = K + (long long)j * dqk;
+    const double *vj = V + (long long)j * dv;
+    for (int i = 0; i < Tq; i++) {
+      if (!visible(causal, i, j)) continue;
+      const double *qi = Q + (long long)i * dqk;
+      const double *doi = dO + (long long)i * dv;
+      double s = 0.0;
+      for (int c = 0; c < dqk; c++) s += qi[c] * kj[c];
+      double pij = exp(scale * s - LSE[i]);
+      double dpij = 0.0;
+      for (int c = 0; c < dv; c++) dpij += doi[c] * vj[c];
+      double dsij = pij * (dpij - D[i]);
+      for (int c = 0; c < dv; c++) dvr[c] += pij * doi[c];
+      for (int c = 0; c < dqk; c++) dk[c] += scale * dsij * qi[c];
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Number of OpenMP threads a parallel region of this library will use. */
+int oracle_num_threads(void) {
+  int n = 1;
+#pragma omp parallel
+  {
+#pragma omp single
+    {
+#ifdef _OPENMP
+      extern int omp_get_num_threads(void);
+      n = omp_get_num_threads();
+#endif
+    }
+  }
+  return n;
+}

@@ -1,0 +1,331 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Every check here ties the oracle to the mathematics of the pages
+("ops(8)：self-attention 的 CUDA 实现及优化 (下) - 深度分析", §2.1 forward and
+backward formulas, §2.2 CPU reference loop, Appendix A.1-A.3): central finite
+differences of the scalar loss L = sum(O * dO), invariants of the softmax
+Jacobian, closed forms on degenerate inputs, a hand-derived two-token example,
+and an independent route (PyTorch CPU fp64 autograd).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from tests._common import rel_err, to_problems
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _small(n=2, T=16, d=8, dv=None, seed=0, Tk=None):
+    dv = d if dv is None else dv
+    Tk = T if Tk is None else Tk
+    return (_rand((n, T, d), seed), _rand((n, Tk, d), seed + 1),
+            _rand((n, Tk, dv), seed + 2), _rand((n, T, dv), seed + 3))
+
+
+def _fd_grad(oracle, q, k, v, dO, causal, scale, which, idx, h=1e-6, lib=None):
+    """Central difference of L = sum(O * dO) w.r.t. one entry of q, k or v."""
+    args = {"q": q, "k": k, "v": v}
+    plus = {kk: vv.copy() for kk, vv in args.items()}
+    minus = {kk: vv.copy() for kk, vv in args.items()}
+    plus[which][idx] += h
+    minus[which][idx] -= h
+    Op, _, _ = oracle.forward(plus["q"], plus["k"], plus["v"], causal, scale, lib=lib)
+    Om, _, _ = oracle.forward(minus["q"], minus["k"], minus["v"], causal, scale, lib=lib)
+    return float(((np.asarray(Op) - np.asarray(Om)) * dO).sum() / (2 * h))
+
+
+def _torch_reference(q, k, v, dO, causal, scale):
+    """PyTorch CPU fp64 autograd of softmax(s Q K^T + mask) V (independent route)."""
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    kt = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    S = scale * qt @ kt.transpose(-1, -2)
+    if causal:
+        Tq, Tk = S.shape[-2:]
+        mask = torch.ones(Tq, Tk, dtype=torch.bool).triu(1)
+        S = S.masked_fill(mask, float("-inf"))
+    P = torch.softmax(S, dim=-1)
+    O = P @ vt
+    lse = torch.logsumexp(S, dim=-1)
+    O.backward(torch.tensor(dO, dtype=torch.float64))
+    return {"O": O.detach().numpy(), "LSE": lse.detach().numpy(),
+            "dQ": qt.grad.numpy(), "dK": kt.grad.numpy(), "dV": vt.grad.numpy()}
+
+
+# --------------------------------------------------------------------------
+# finite differences
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_finite_differences_every_entry(oracle_mod, causal):
+    """Every entry of dQ, dK, dV at T=16, d=8, H=2 against central differences."""
+    q, k, v, dO = _small(n=2, T=16, d=8)
+    scale = 0.35
+    g = oracle_mod.backward(q, k, v, dO, causal, scale)
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            fd[idx] = _fd_grad(oracle_mod, q, k, v, dO, causal, scale, which, idx)
+        err = np.max(np.abs(fd - grad)) / max(np.max(np.abs(grad)), 1e-30)
+        assert err <= 1e-7, (which, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_finite_differences_tiny_config_sampled(oracle_mod, causal):
+    """256 seeded entries per tensor on the tiny workload (bf16 inputs, d=64)."""
+    from attention_backward_flashattention_gb300 import synthetic as syn
+    w = syn.TINY[1] if causal else syn.TINY[0]
+    x = syn.make_inputs(w)
+    q, k, v, dO = (to_problems(x[n]) for n in ("q", "k", "v", "dO"))
+    g = oracle_mod.backward(q, k, v, dO, causal, w.scale)
+    rng = np.random.default_rng(7)
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        flat = rng.choice(grad.size, size=256, replace=False)
+        scale_ref = np.max(np.abs(grad))
+        worst = 0.0
+        for f in flat:
+            idx = np.unravel_index(f, grad.shape)
+            fd = _fd_grad(oracle_mod, q, k, v, dO, causal, w.scale, which, idx)
+            worst = max(worst, abs(fd - grad[idx]) / scale_ref)
+        assert worst <= 1e-7, (which, worst)
+
+
+# --------------------------------------------------------------------------
+# invariants
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_jacobian_invariants(oracle_mod, causal):
+    q, k, v, dO = _small(n=3, T=24, d=16, dv=8, seed=11)
+    s = 0.25
+    r = oracle_mod.backward(q, k, v, dO, causal, s, mode="E", want_matrices=True)
+    P, dS = r["P"], r["dS"]
+    # rows of P sum to one; rows of dS sum to zero (J 1 = 0)
+    assert np.max(np.abs(P.sum(-1) - 1.0)) <= 1e-13
+    assert np.max(np.abs(dS.sum(-1))) <= 1e-12 * np.linalg.norm(dS)
+    # D = rowsum(dO * O) = rowsum(P * dP)
+    dP = dO @ v.transpose(0, 2, 1)
+    D_def = (P * dP).sum(-1)
+    D_io = (dO * r["O"]).sum(-1)
+    assert rel_err(r["D"], D_def) <= 1e-12
+    assert rel_err(D_io, D_def) <= 1e-12
+    # dV = P^T dO from the explicitly formed P; dQ, dK from the explicit dS
+    assert rel_err(r["dV"], P.transpose(0, 2, 1) @ dO) <= 1e-12
+    assert rel_err(r["dQ"], s * dS @ k) <= 1e-12
+    assert rel_err(r["dK"], s * dS.transpose(0, 2, 1) @ q) <= 1e-12
+    # O = P V and LSE from the explicit P
+    assert rel_err(r["O"], P @ v) <= 1e-12
+    if causal:
+        upper = np.triu(np.ones(P.shape[-2:], dtype=bool), 1)
+        assert np.all(P[:, upper] == 0.0) and np.all(dS[:, upper] == 0.0)
+
+
+def test_causal_masking_properties(oracle_mod):
+    q, k, v, dO = _small(n=2, T=20, d=8, seed=21)
+    s = 0.4
+    T = q.shape[1]
+    r = oracle_mod.backward(q, k, v, dO, True, s, mode="E", want_matrices=True)
+    # the last key is seen by the last query only
+    P, dS = r["P"], r["dS"]
+    assert rel_err(r["dV"][:, -1], P[:, -1, -1, None] * dO[:, -1]) <= 1e-13
+    assert rel_err(r["dK"][:, -1], s * dS[:, -1, -1, None] * q[:, -1]) <= 1e-13
+    # perturbing keys / values above the diagonal leaves earlier rows unchanged
+    O0, L0, _ = oracle_mod.forward(q, k, v, True, s)
+    for i in (0, 5, 13):
+        k2, v2 = k.copy(), v.copy()
+        k2[:, i + 1:] += _rand(k2[:, i + 1:].shape, 99)
+        v2[:, i + 1:] += _rand(v2[:, i + 1:].shape, 98)
+        O1, L1, _ = oracle_mod.forward(q, k2, v2, True, s)
+        assert np.array_equal(O1[:, :i + 1], O0[:, :i + 1])
+        assert np.array_equal(L1[:, :i + 1], L0[:, :i + 1])
+    # the last query row sees every key: causal and non-causal agree there
+    Onc, Lnc, _ = oracle_mod.forward(q, k, v, False, s)
+    assert rel_err(O0[:, T - 1], Onc[:, T - 1]) <= 1e-14
+    assert rel_err(L0[:, T - 1], Lnc[:, T - 1]) <= 1e-14
+    # gradients only flow to keys at or before the query
+    rows = [np.array([7]), np.array([7])]
+    rr = oracle_mod.backward(q, k, v, dO, True, s, rows=rows)
+    assert np.all(rr["dK"][:, 8:] == 0.0) and np.all(rr["dV"][:, 8:] == 0.0)
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+def test_single_token(oracle_mod):
+    """T=1: O=V, LSE=s q.k, dV=dO, dQ=dK=0 (softmax of one score is 1)."""
+    q, k, v, dO = _small(n=4, T=1, d=8, dv=5, seed=3)
+    s = 0.7
+    for causal in (False, True):
+        r = oracle_mod.backward(q, k, v, dO, causal, s)
+        assert np.allclose(r["O"], v, rtol=0, atol=1e-15)
+        assert np.allclose(r["LSE"][:, 0], s * (q[:, 0] * k[:, 0]).sum(-1), rtol=1e-15, atol=0)
+        assert np.allclose(r["dV"], dO, rtol=0, atol=1e-15)
+        assert np.max(np.abs(r["dQ"])) <= 1e-15 and np.max(np.abs(r["dK"])) <= 1e-15
+
+
+def test_uniform_attention(oracle_mod):
+    """Q = 0, non-causal: every score is 0, so P = 1/T."""
+    _, k, v, dO = _small(n=2, T=12, d=6, dv=4, seed=5)
+    q = np.zeros_like(k)
+    T = k.shape[1]
+    r = oracle_mod.backward(q, k, v, dO, False, 0.5)
+    assert rel_err(r["O"], np.broadcast_to(v.mean(1, keepdims=True), r["O"].shape)) <= 1e-14
+    assert np.allclose(r["LSE"], math.log(T), rtol=1e-15, atol=0)
+    assert rel_err(r["dV"], np.broadcast_to(dO.sum(1, keepdims=True) / T, r["dV"].shape)) <= 1e-14
+    # dK = s dS^T Q = 0 when Q = 0
+    assert np.max(np.abs(r["dK"])) == 0.0
+
+
+def test_causal_first_row(oracle_mod):
+    """Causal row 0 sees key 0 only: O_0 = V_0, LSE_0 = s q_0.k_0, dQ_0 = 0."""
+    q, k, v, dO = _small(n=2, T=9, d=8, seed=8)
+    s = 0.3
+    r = oracle_mod.backward(q, k, v, dO, True, s)
+    assert np.allclose(r["O"][:, 0], v[:, 0], rtol=0, atol=1e-15)
+    assert np.allclose(r["LSE"][:, 0], s * (q[:, 0] * k[:, 0]).sum(-1), rtol=1e-15, atol=0)
+    assert np.max(np.abs(r["dQ"][:, 0])) <= 1e-15
+
+
+def _golden_value(expr):
+    """Evaluate a fixture entry such as '3*ln3/16' (ln2/ln3/ln4 and rationals only)."""
+    env = {"ln2": math.log(2.0), "ln3": math.log(3.0), "ln4": math.log(4.0)}
+    return float(eval(expr, {"__builtins__": {}}, env))
+
+
+def _golden(name):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    with open(path) as f:
+        return json.load(f)
+
+
+def test_hand_derived_two_token_example(oracle_mod):
+    """Two tokens, d=1, s=1, worked by hand (tests/golden/two_token_example.json)."""
+    g = _golden("two_token_example.json")
+    ev = lambda a: np.vectorize(_golden_value, otypes=[float])(np.array(a))
+    inp = g["inputs"]
+    q, k, v, dO = (ev(inp[n]).reshape(1, 2, 1) for n in ("q", "k", "v", "dO"))
+    exp = {key: ev(val) for key, val in g["expected"].items()}
+    for mode in ("R", "E"):
+        r = oracle_mod.backward(q, k, v, dO, inp["causal"], inp["scale"], mode=mode,
+                                want_matrices=True)
+        np.testing.assert_allclose(r["O"][0, :, 0], exp["O"], rtol=1e-15)
+        np.testing.assert_allclose(r["LSE"][0], exp["LSE"], rtol=1e-15)
+        np.testing.assert_allclose(r["D"][0], exp["D"], rtol=1e-15)
+        np.testing.assert_allclose(r["dS"][0], exp["dS"], rtol=1e-14)
+        np.testing.assert_allclose(r["dQ"][0, :, 0], exp["dQ"], rtol=1e-14)
+        np.testing.assert_allclose(r["dK"][0, :, 0], exp["dK"], rtol=1e-14)
+        np.testing.assert_allclose(r["dV"][0, :, 0], exp["dV"], rtol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# two backward forms and an independent route
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_jacobian_and_rowjvp_agree_tiny(oracle_mod, causal):
+    from attention_backward_flashattention_gb300 import synthetic as syn
+    w = syn.TINY[1] if causal else syn.TINY[0]
+    x = syn.make_inputs(w)
+    q, k, v, dO = (to_problems(x[n]) for n in ("q", "k", "v", "dO"))
+    rE = oracle_mod.backward(q, k, v, dO, causal, w.scale, mode="E")
+    rR = oracle_mod.backward(q, k, v, dO, causal, w.scale, mode="R")
+    for key in ("dQ", "dK", "dV"):
+        assert rel_err(rR[key], rE[key]) <= 1e-12, key
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_torch_autograd_route_tiny(oracle_mod, causal):
+    from attention_backward_flashattention_gb300 import synthetic as syn
+    w = syn.TINY[1] if causal else syn.TINY[0]
+    x = syn.make_inputs(w)
+    q, k, v, dO = (to_problems(x[n]) for n in ("q", "k", "v", "dO"))
+    r = oracle_mod.backward(q, k, v, dO, causal, w.scale)
+    t = _torch_reference(q, k, v, dO, causal, w.scale)
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(r[key], t[key]) <= 1e-10, key
+    assert np.max(np.abs(r["LSE"] - t["LSE"])) <= 1e-12
+
+
+def test_gpt2_shaped_heads_against_autograd_and_jacobian(oracle_mod):
+    """A seeded subset of (batch, head) problems of the GPT-2-shaped layer."""
+    from attention_backward_flashattention_gb300 import synthetic as syn
+    w = syn.GPT2
+    x = syn.make_inputs(w)
+    q, k, v, dO = (to_problems(x[n]) for n in ("q", "k", "v", "dO"))
+    pick = np.random.default_rng(1).choice(q.shape[0], size=3, replace=False)
+    q, k, v, dO = q[pick], k[pick], v[pick], dO[pick]
+    r = oracle_mod.backward(q, k, v, dO, True, w.scale)
+    t = _torch_reference(q, k, v, dO, True, w.scale)
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(r[key], t[key]) <= 1e-10, key
+    assert np.max(np.abs(r["LSE"] - t["LSE"])) <= 1e-11
+    rE = oracle_mod.backward(q[:1], k[:1], v[:1], dO[:1], True, w.scale, mode="E")
+    for key in ("dQ", "dK", "dV"):
+        assert rel_err(r[key][:1], rE[key]) <= 1e-12, key
+
+
+# --------------------------------------------------------------------------
+# the sampled entry points used at full sizes agree with the full oracle
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_and_column_sampling_matches_full(oracle_mod, causal):
+    q, k, v, dO = _small(n=2, T=40, d=16, dv=8, seed=31)
+    s = 0.25
+    full = oracle_mod.backward(q, k, v, dO, causal, s)
+    rows = [np.array([0, 3, 39]), np.array([17, 39])]
+    part = oracle_mod.backward(q, k, v, dO, causal, s, rows=rows)
+    for p, rr in enumerate(rows):
+        for key in ("dQ", "O", "LSE", "D"):
+            np.testing.assert_allclose(part[key][p][rr], full[key][p][rr], rtol=1e-14, atol=1e-15)
+    O, lse, D = oracle_mod.forward(q, k, v, causal, s, dO=dO)
+    np.testing.assert_allclose(D, full["D"], rtol=1e-13, atol=1e-15)
+    keys = np.array([0, 1, 20, 39])
+    for p in range(2):
+        dk, dvv = oracle_mod.kv_rows(q[p], k[p], v[p], dO[p], lse[p], D[p], keys, causal, s)
+        np.testing.assert_allclose(dk, full["dK"][p][keys], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dvv, full["dV"][p][keys], rtol=1e-11, atol=1e-13)
+    # the row-sampled dK/dV contributions of all rows add up to the full gradient
+    halves = [[np.arange(0, 20), np.arange(0, 20)], [np.arange(20, 40), np.arange(20, 40)]]
+    a = oracle_mod.backward(q, k, v, dO, causal, s, rows=halves[0])
+    b = oracle_mod.backward(q, k, v, dO, causal, s, rows=halves[1])
+    assert rel_err(a["dK"] + b["dK"], full["dK"]) <= 1e-13
+    assert rel_err(a["dV"] + b["dV"], full["dV"]) <= 1e-13
+
+
+def test_unequal_lengths_are_independent_problems(oracle_mod):
+    lens = [5, 17, 1, 9]
+    parts = [_small(n=1, T=L, d=8, seed=40 + i) for i, L in enumerate(lens)]
+    q = [p[0][0] for p in parts]
+    k = [p[1][0] for p in parts]
+    v = [p[2][0] for p in parts]
+    dO = [p[3][0] for p in parts]
+    r = oracle_mod.backward(q, k, v, dO, True, 0.3)
+    for i in range(len(lens)):
+        ri = oracle_mod.backward(q[i][None], k[i][None], v[i][None], dO[i][None], True, 0.3)
+        for key in ("dQ", "dK", "dV", "O", "LSE"):
+            np.testing.assert_array_equal(r[key][i], ri[key][0])
+
+
+def test_noncausal_rectangular(oracle_mod):
+    """Tq != Tk is defined for the non-causal case; FD on a few entries."""
+    q, k, v, dO = _small(n=1, T=7, d=4, seed=50, Tk=11)
+    s = 0.6
+    g = oracle_mod.backward(q, k, v, dO, False, s)
+    t = _torch_reference(q, k, v, dO, False, s)
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(g[key], t[key]) <= 1e-12
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        idx = (0, 2, 1)
+        assert abs(_fd_grad(oracle_mod, q, k, v, dO, False, s, which, idx) - grad[idx]) <= 1e-8
+
+
+def test_rejects_causal_rectangular(oracle_mod):
+    q, k, v, dO = _small(n=1, T=7, d=4, seed=50, Tk=11)
+    with pytest.raises(ValueError):
+        oracle_mod.backward(q, k, v, dO, True, 0.5)
