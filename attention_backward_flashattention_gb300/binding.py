@@ -1,0 +1,225 @@
+"""ctypes binding of the C ABI in ``include/attn.h`` (libattn_gb300.so).
+
+The functions named like the C entry points (``attn_fwd``, ``attn_bwd``, ...)
+only marshal arguments: tensors become device pointers, streams become
+``cudaStream_t`` handles, and the integer status comes back unchanged.
+``forward`` / ``backward`` are conveniences on top that allocate outputs and
+the workspace with PyTorch (device memory only) and raise ``AttnError`` on a
+non-zero status.  Every step of the computation runs in the library's CUDA
+kernels: there is no CPU path, and a missing library raises at first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libattn_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_WORKSPACE_TOO_SMALL = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+LAYOUT_BTHD = 0
+LAYOUT_PACKED_QKV = 1
+MAX_VARLEN_SEQS = 1024
+
+EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
+            "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+        self.code = code
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m attention_backward_flashattention_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, P]
+        lib.attn_fwd.restype = I
+        lib.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        lib.attn_bwd_workspace_size.restype = SZ
+        lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P,
+                                 SZ, P]
+        lib.attn_bwd.restype = I
+        lib.attn_bwd_status.argtypes = [P, P]
+        lib.attn_bwd_status.restype = I
+        lib.attn_fwd_status.argtypes = [P]
+        lib.attn_fwd_status.restype = I
+        lib.attn_strerror.argtypes = [I]
+        lib.attn_strerror.restype = ctypes.c_char_p
+        lib.attn_varlen_order.argtypes = [P, I, P]
+        lib.attn_varlen_order.restype = I
+        lib.attn_debug_set_wait_bias.argtypes = [I]
+        lib.attn_debug_set_wait_bias.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream
+    return int(s)
+
+
+class _HostInts:
+    """Keeps a host int32 array alive for the duration of a call."""
+
+    def __init__(self, values):
+        if values is None:
+            self.arr = None
+        else:
+            vals = [int(v) for v in (values.tolist() if hasattr(values, "tolist") else values)]
+            self.arr = (ctypes.c_int * len(vals))(*vals)
+
+    @property
+    def ptr(self):
+        return None if self.arr is None else ctypes.cast(self.arr, ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------
+# C entry points (same names, argument marshalling only)
+# ----------------------------------------------------------------------------
+def attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, scale, cu_seqlens=None,
+             layout=LAYOUT_BTHD, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, dqk, dv,
+                           int(causal), float(scale), cu.ptr, layout, _stream(stream))
+
+
+def attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen=False, deterministic=False) -> int:
+    return int(load().attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, int(varlen),
+                                              int(deterministic)))
+
+
+def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal, scale,
+             cu_seqlens=None, layout=LAYOUT_BTHD, deterministic=False, workspace=None,
+             workspace_bytes=0, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                           _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv, int(causal),
+                           float(scale), cu.ptr, layout, int(deterministic), _ptr(workspace),
+                           int(workspace_bytes), _stream(stream))
+
+
+def attn_bwd_status(workspace, stream=None) -> int:
+    return load().attn_bwd_status(_ptr(workspace), _stream(stream))
+
+
+def attn_fwd_status(stream=None) -> int:
+    return load().attn_fwd_status(_stream(stream))
+
+
+def attn_strerror(code: int) -> str:
+    return load().attn_strerror(int(code)).decode()
+
+
+def strerror(code: int) -> str:
+    try:
+        return attn_strerror(code)
+    except RuntimeError:
+        return f"code {code}"
+
+
+def attn_debug_set_wait_bias(bias: int) -> int:
+    return load().attn_debug_set_wait_bias(int(bias))
+
+
+def attn_varlen_order(cu_seqlens) -> list:
+    cu = _HostInts(cu_seqlens)
+    n = len(cu.arr) - 1
+    out = (ctypes.c_int * max(n, 1))()
+    rc = load().attn_varlen_order(cu.ptr, n, ctypes.cast(out, ctypes.c_void_p))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_varlen_order")
+    return list(out)[:n]
+
+
+# ----------------------------------------------------------------------------
+# Conveniences: shapes from tensors, outputs allocated with torch
+# ----------------------------------------------------------------------------
+def _dims(q, k, v, cu_seqlens, layout):
+    if layout == LAYOUT_PACKED_QKV:
+        # q, k, v are slot views of one (..., 3, H, d) buffer
+        H, dqk = q.shape[-2], q.shape[-1]
+        dv = v.shape[-1]
+    else:
+        H, dqk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    if cu_seqlens is not None:
+        B = len(cu_seqlens) - 1
+        Tq, Tk = q.shape[0], k.shape[0]
+    else:
+        B, Tq, Tk = q.shape[0], q.shape[1], k.shape[1]
+    return B, H, Tq, Tk, dqk, dv
+
+
+def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BTHD,
+            with_lse=True, stream=None):
+    """O (bf16, like q with v's head size) and LSE (fp32) or None."""
+    B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
+    scale = 1.0 / math.sqrt(dqk) if scale is None else scale
+    o = torch.empty(q.shape[:-2] + (H, dv), dtype=torch.bfloat16, device=q.device)
+    lse = None
+    if with_lse:
+        lse = torch.empty((H, Tq) if cu_seqlens is not None else (B, H, Tq),
+                          dtype=torch.float32, device=q.device)
+    rc = attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, scale, cu_seqlens, layout,
+                  stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
+             layout=LAYOUT_BTHD, deterministic=False, workspace=None, stream=None, out=None):
+    """(dq, dk, dv) as bf16 tensors shaped like q, k, v (a packed buffer for layout 1)."""
+    B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
+    scale = 1.0 / math.sqrt(dqk) if scale is None else scale
+    if out is not None:
+        dq, dk, dvt = out
+    elif layout == LAYOUT_PACKED_QKV:
+        g = torch.empty(q.shape[:-2] + (3, H, dqk), dtype=torch.bfloat16, device=q.device)
+        dq, dk, dvt = g.select(-3, 0), g.select(-3, 1), g.select(-3, 2)
+    else:
+        dq = torch.empty_like(q)
+        dk = torch.empty_like(k)
+        dvt = torch.empty_like(v)
+    need = attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, cu_seqlens is not None, deterministic)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = attn_bwd(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, scale,
+                  cu_seqlens, layout, deterministic, workspace,
+                  workspace.numel() * workspace.element_size(), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dvt

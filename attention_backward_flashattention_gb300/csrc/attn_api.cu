@@ -1,0 +1,346 @@
+// attn_api.cu — the C ABI of include/attn.h: argument validation, layouts,
+// workspace carving, variable-length schedule tables, TMA tensor maps and the
+// launches.  Everything here is host code; all arithmetic runs in the kernels
+// of attn_fwd.cu and attn_bwd.cu.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+#include "tmap.h"
+
+using namespace attn;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+}
+
+int num_sms_current() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> g(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Common shape checks of attn_fwd / attn_bwd.  Returns ATTN_OK or an error.
+int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const int* cu,
+                int layout) {
+  if (B <= 0 || H <= 0 || Tq <= 0 || Tk <= 0) return ATTN_ERR_INVALID_ARG;
+  if (layout != ATTN_LAYOUT_BTHD && layout != ATTN_LAYOUT_PACKED_QKV) return ATTN_ERR_INVALID_ARG;
+  if (!supported_dims(dqk, dv)) return ATTN_ERR_UNSUPPORTED;
+  if (layout == ATTN_LAYOUT_PACKED_QKV && (dqk != dv || Tq != Tk)) return ATTN_ERR_UNSUPPORTED;
+  if (cu != nullptr) {
+    if (B > ATTN_MAX_VARLEN_SEQS) return ATTN_ERR_UNSUPPORTED;
+    if (Tq != Tk) return ATTN_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[B] != Tq) return ATTN_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b)
+      if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
+  } else {
+    if (causal && Tq != Tk) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)B * Tq > INT32_MAX || (int64_t)B * Tk > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+  }
+  // every row of every tensor must fit the 32-bit coordinates of the TMA maps
+  if ((int64_t)H * 3 * dqk > (1 << 20)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int order_impl(const int* cu, int nseq, int* order) {
+  if (cu == nullptr || order == nullptr || nseq <= 0 || nseq > ATTN_MAX_VARLEN_SEQS)
+    return ATTN_ERR_INVALID_ARG;
+  for (int b = 0; b < nseq; ++b) {
+    if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
+    order[b] = b;
+  }
+  std::stable_sort(order, order + nseq, [cu](int a, int b) {
+    return (cu[a + 1] - cu[a]) > (cu[b + 1] - cu[b]);
+  });
+  return ATTN_OK;
+}
+
+// Variable-length tables: sequences longest first; items per sequence are
+// (tiles of that sequence) x H; q-tiles numbered sequence by sequence.
+void build_tables(const int* cu, int nseq, int H, VarlenTables* t, int* n_items, int* n_qtiles) {
+  std::memset(t, 0, sizeof(*t));
+  for (int b = 0; b <= nseq; ++b) t->cu[b] = cu[b];
+  order_impl(cu, nseq, t->order);
+  int acc = 0;
+  for (int k = 0; k < nseq; ++k) {
+    t->item_start[k] = acc;
+    const int s = t->order[k];
+    acc += cdiv(cu[s + 1] - cu[s], kTile) * H;
+  }
+  t->item_start[nseq] = acc;
+  *n_items = acc;
+  int tiles = 0;
+  for (int s = 0; s < nseq; ++s) {
+    t->tile_start[s] = tiles;
+    tiles += cdiv(cu[s + 1] - cu[s], kTile);
+  }
+  t->tile_start[nseq] = tiles;
+  *n_qtiles = tiles;
+}
+
+struct Layout {
+  int64_t q_row, k_row, v_row;   // element distance between token rows of q / k / v
+  int64_t o_row;                 // ... of o and dO
+  int64_t g_q_row, g_k_row, g_v_row;  // ... of dq / dk / dv
+};
+
+Layout make_layout(int layout, int H, int dqk, int dv) {
+  Layout L;
+  if (layout == ATTN_LAYOUT_PACKED_QKV) {
+    const int64_t r = 3ll * H * dqk;
+    L.q_row = L.k_row = L.v_row = r;
+    L.g_q_row = L.g_k_row = L.g_v_row = r;
+  } else {
+    L.q_row = L.k_row = L.g_q_row = L.g_k_row = (int64_t)H * dqk;
+    L.v_row = L.g_v_row = (int64_t)H * dv;
+  }
+  L.o_row = (int64_t)H * dv;
+  return L;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsSizes {
+  size_t header, sem, stat, acc, total;
+};
+
+WsSizes ws_sizes(int n_qtiles, int H, int dqk) {
+  WsSizes w;
+  w.header = 256;
+  w.sem = round256((size_t)n_qtiles * H * sizeof(int));
+  w.stat = round256((size_t)n_qtiles * H * kTile * sizeof(float));
+  w.acc = round256((size_t)n_qtiles * H * kTile * dqk * sizeof(float));
+  w.total = w.header + w.sem + 2 * w.stat + w.acc;
+  return w;
+}
+
+int qtiles_bound(int B, int Tq, bool varlen) {
+  return varlen ? cdiv(Tq, kTile) + B : B * cdiv(Tq, kTile);
+}
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Host-side fault injection (tests only): added to every ordered-dQ wait
+// target of deterministic backward calls, so that the wait can never succeed.
+std::atomic<int> g_sem_bias{0};
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown error";
+  }
+}
+
+int attn_varlen_order(const int* cu_seqlens, int nseq, int* order_out) {
+  return order_impl(cu_seqlens, nseq, order_out);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int dqk, int dv, int varlen,
+                               int deterministic) {
+  (void)deterministic;
+  (void)Tk;
+  if (B <= 0 || H <= 0 || Tq <= 0 || !supported_dims(dqk, dv)) return 0;
+  return ws_sizes(qtiles_bound(B, Tq, varlen != 0), H, dqk).total;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Tq, int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
+             int layout, void* stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout);
+  if (rc) return rc;
+
+  FwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  static thread_local VarlenTables tables;
+  const bool varlen = cu_seqlens != nullptr;
+  const Layout lay = make_layout(layout, H, dqk, dv);
+  const int64_t rows_q = varlen ? Tq : (int64_t)B * Tq;
+  const int64_t rows_k = varlen ? Tk : (int64_t)B * Tk;
+  if (!make_panel_map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
+      !make_panel_map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
+      !make_panel_map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile))
+    return ATTN_ERR_CUDA;
+  L.sh.nseq = B;
+  L.sh.H = H;
+  L.sh.varlen = varlen ? 1 : 0;
+  L.sh.Tq = Tq;
+  L.sh.Tk = Tk;
+  L.sh.nq_tiles = cdiv(Tq, kTile);
+  L.sh.nk_tiles = cdiv(Tk, kTile);
+  L.sh.causal = causal ? 1 : 0;
+  L.sh.descending = 0;
+  if (varlen) {
+    int n_items = 0, n_qt = 0;
+    build_tables(cu_seqlens, B, H, &tables, &n_items, &n_qt);
+    L.sh.n_items = n_items;
+    L.tables = &tables;
+    L.lse_head_stride = Tq;
+    L.lse_seq_stride = 0;
+  } else {
+    L.sh.n_items = B * H * L.sh.nq_tiles;
+    L.tables = nullptr;
+    L.lse_head_stride = Tq;
+    L.lse_seq_stride = (int64_t)H * Tq;
+  }
+  if (L.sh.n_items == 0) return ATTN_OK;
+  L.o = o;
+  L.lse = lse;
+  L.o_row_stride = lay.o_row;
+  L.scale_log2 = scale * kLog2e;
+  L.status = fwd_status_ptr();
+  if (!L.status) return ATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  L.grid = std::min(L.sh.n_items, sms);
+  L.stream = static_cast<cudaStream_t>(stream);
+  return cuda_err(launch_fwd(L, dqk, dv));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
+             int dqk, int dv, int causal, float scale, const int* cu_seqlens, int layout,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv_out || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv_out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout);
+  if (rc) return rc;
+  const bool varlen = cu_seqlens != nullptr;
+  if (workspace_bytes < attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen, deterministic))
+    return ATTN_ERR_WORKSPACE_TOO_SMALL;
+
+  BwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  static thread_local VarlenTables tables;
+  const Layout lay = make_layout(layout, H, dqk, dv);
+  const int64_t rows_q = varlen ? Tq : (int64_t)B * Tq;
+  const int64_t rows_k = varlen ? Tk : (int64_t)B * Tk;
+  if (!make_panel_map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
+      !make_panel_map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
+      !make_panel_map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile) ||
+      !make_panel_map(&L.tm_do, dO, dv, H, rows_q, dv, lay.o_row, kTile))
+    return ATTN_ERR_CUDA;
+  L.sh.nseq = B;
+  L.sh.H = H;
+  L.sh.varlen = varlen ? 1 : 0;
+  L.sh.Tq = Tq;
+  L.sh.Tk = Tk;
+  L.sh.nq_tiles = cdiv(Tq, kTile);
+  L.sh.nk_tiles = cdiv(Tk, kTile);
+  L.sh.causal = causal ? 1 : 0;
+  L.sh.descending = deterministic ? 1 : 0;
+  int n_qtiles;
+  if (varlen) {
+    int n_items = 0;
+    build_tables(cu_seqlens, B, H, &tables, &n_items, &n_qtiles);
+    L.sh.n_items = n_items;
+    L.tables = &tables;
+    L.lse_head_stride = Tq;
+    L.lse_seq_stride = 0;
+  } else {
+    L.sh.n_items = B * H * L.sh.nk_tiles;
+    n_qtiles = B * L.sh.nq_tiles;
+    L.tables = nullptr;
+    L.lse_head_stride = Tq;
+    L.lse_seq_stride = (int64_t)H * Tq;
+  }
+  if (L.sh.n_items == 0) return ATTN_OK;
+  // carve the workspace (sizes from the bound, offsets fixed by the query)
+  const WsSizes w = ws_sizes(qtiles_bound(B, Tq, varlen), H, dqk);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  L.ws.header = reinterpret_cast<int*>(base);
+  L.ws.sem = reinterpret_cast<int*>(base + w.header);
+  L.ws.lse2 = reinterpret_cast<float*>(base + w.header + w.sem);
+  L.ws.dsum = reinterpret_cast<float*>(base + w.header + w.sem + w.stat);
+  L.ws.dq_acc = reinterpret_cast<float*>(base + w.header + w.sem + 2 * w.stat);
+  L.o = o;
+  L.dout = dO;
+  L.lse = lse;
+  L.dq = dq;
+  L.dk = dk;
+  L.dv = dv_out;
+  L.q_row_stride = lay.q_row;
+  L.k_row_stride = lay.k_row;
+  L.v_row_stride = lay.v_row;
+  L.o_row_stride = lay.o_row;
+  L.do_row_stride = lay.o_row;
+  L.dq_row_stride = lay.g_q_row;
+  L.dk_row_stride = lay.g_k_row;
+  L.dv_row_stride = lay.g_v_row;
+  L.scale = scale;
+  L.scale_log2 = scale * kLog2e;
+  L.n_qtiles = n_qtiles;
+  L.deterministic = deterministic ? 1 : 0;
+  L.sem_bias = g_sem_bias.load();
+  const int sms = num_sms_current();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  L.num_sms = sms;
+  L.grid = std::min(L.sh.n_items, sms);
+  L.stream = static_cast<cudaStream_t>(stream);
+  return cuda_err(launch_bwd(L, dqk, dv));
+}
+
+int attn_debug_set_wait_bias(int bias) {
+  g_sem_bias.store(bias);
+  return ATTN_OK;
+}
+
+int attn_bwd_status(const void* workspace, void* stream) {
+  if (!workspace) return ATTN_ERR_INVALID_ARG;
+  int st = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  return st;
+}
+
+int attn_fwd_status(void* stream) {
+  int* p = fwd_status_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  int st = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&st, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,770 @@
+// attn_bwd.cu — fused attention backward for sm_103a.
+//
+// The chain rule of "ops(8)：self-attention 的 CUDA 实现及优化 (下) - 深度分析"
+// §2.1 (dV = P^T dO, dP = dO V^T, dS = P ⊙ (dP - rowsum(dP ⊙ P)),
+// dQ = dS K / sqrt(d_k), dK = dS^T Q / sqrt(d_k)), with the row sum taken as
+// D = rowsum(dO ⊙ O) (the simplification §2.3 V7 and §5.3 allude to: the two
+// are equal because O = P V), P recomputed from Q, K and the forward's LSE
+// instead of being stored, and dQ reduced across key tiles as in
+// "深度学习反向传播优化：2-CTA MMA模式与内存访问优化" §3 (global fp32 atomics, or
+// a semaphore-ordered deterministic variant, §3.2).
+//
+// Three launches per call, all on the caller's stream:
+//   1. attn_bwd_pre_kernel   (memory-bound) D = rowsum(dO ⊙ O) and LSE·log2(e)
+//      into padded per-tile workspace rows; zero the fp32 dQ accumulator, the
+//      semaphores, the work counter and the status word.
+//   2. attn_bwd_main_kernel  one CTA per SM, persistent; each work item is one
+//      128-key tile of one (sequence, head).  K_j and V_j stay in shared
+//      memory, dK_j and dV_j accumulate in tensor memory, and the loop walks
+//      the query tiles i:
+//         S^T  = K_j Q_i^T                    (MMA, TMEM)
+//         P^T  = exp2(S^T·s·log2e − LSE2_i)   (compute warps)
+//         dP^T = V_j dO_i^T                   (MMA, TMEM)
+//         dV_j += P^T dO_i                    (MMA)
+//         dS^T = P^T ⊙ (dP^T − D_i)           (compute warps, bf16 to smem)
+//         dK_j += dS^T Q_i                    (MMA)
+//         dQ_i  = dS K_j                      (MMA, TMEM) -> fp32 reduction
+//      Working transposed (keys on TMEM lanes) makes P^T and dS^T the natural
+//      A operands of the dV and dK products; dQ reads the same dS^T tile
+//      through an MN-major descriptor.
+//   3. attn_bwd_convert_kernel  dQ = bf16(s · dQacc) into the caller's layout.
+//
+// Roles in the main kernel (320 threads):
+//   warps 0-3, 4-7  compute warpgroups; thread = key row (TMEM lane); group g
+//                   handles query columns [64g, 64g+64) of S^T/dP^T and half
+//                   of the dQ / dK / dV columns in the reductions and epilogue
+//   warp 8          TMA producer and work-item claimer
+//   warp 9          MMA issuer, tensor-memory owner
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kPanelBytes = kTile * 128;
+constexpr int kMaxSmem = 232448;
+constexpr int kMainThreads = 320;
+constexpr int kComputeThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// Sequence helpers (shared by the memory-bound kernels)
+// ---------------------------------------------------------------------------
+template <typename Tables>
+struct SeqOf;
+
+template <>
+struct SeqOf<NoTables> {
+  // token row -> (sequence, position); sequences have length Tq
+  __device__ static void locate(const SeqShape& sh, const NoTables&, int row, int& s, int& t) {
+    s = row / sh.Tq;
+    t = row - s * sh.Tq;
+  }
+  __device__ static int length(const SeqShape& sh, const NoTables&, int) { return sh.Tq; }
+  __device__ static int row0(const SeqShape& sh, const NoTables&, int s) { return s * sh.Tq; }
+  __device__ static int tile_start(const SeqShape& sh, const NoTables&, int s) {
+    return s * sh.nq_tiles;
+  }
+  // workspace q-tile g -> (sequence, tile within it)
+  __device__ static void tile_of(const SeqShape& sh, const NoTables&, int g, int& s, int& i) {
+    s = g / sh.nq_tiles;
+    i = g - s * sh.nq_tiles;
+  }
+};
+
+template <>
+struct SeqOf<VarlenTables> {
+  __device__ static void locate(const SeqShape& sh, const VarlenTables& tb, int row, int& s,
+                                int& t) {
+    int lo = 0, hi = sh.nseq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tb.cu[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    s = lo;
+    t = row - tb.cu[lo];
+  }
+  __device__ static int length(const SeqShape&, const VarlenTables& tb, int s) {
+    return tb.cu[s + 1] - tb.cu[s];
+  }
+  __device__ static int row0(const SeqShape&, const VarlenTables& tb, int s) { return tb.cu[s]; }
+  __device__ static int tile_start(const SeqShape&, const VarlenTables& tb, int s) {
+    return tb.tile_start[s];
+  }
+  __device__ static void tile_of(const SeqShape& sh, const VarlenTables& tb, int g, int& s,
+                                 int& i) {
+    int lo = 0, hi = sh.nseq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tb.tile_start[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    s = lo;
+    i = g - tb.tile_start[lo];
+  }
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// 1. preprocess
+// ---------------------------------------------------------------------------
+template <int DQK, int DV, typename Tables>
+__global__ void __launch_bounds__(256)
+    attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                        const float* __restrict__ lse, const int64_t o_row_stride,
+                        const int64_t do_row_stride, const int64_t lse_head_stride,
+                        const int64_t lse_seq_stride, const int total_rows, const int n_qtiles,
+                        BwdWorkspace ws, const SeqShape sh, const __grid_constant__ Tables tb) {
+  using S = SeqOf<Tables>;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int H = sh.H;
+  if (tid == 0) {
+    ws.header[0] = 0;  // status
+    ws.header[1] = 0;  // work-item counter
+  }
+  for (int64_t i = tid; i < (int64_t)n_qtiles * H; i += nthreads) ws.sem[i] = 0;
+
+  // D and LSE*log2(e) for every real (token, head) row: DV/8 threads per row,
+  // 16 bytes each, consecutive threads along the row (coalesced).
+  constexpr int kTPR = DV / 8;  // threads per row: 8 or 16 (a power of two)
+  const int64_t n_work = (int64_t)total_rows * H * kTPR;
+  // round the loop bound up so that every lane of a row group iterates together
+  const int64_t n_loop = (n_work + nthreads - 1) / nthreads * nthreads;
+  for (int64_t w = tid; w < n_loop; w += nthreads) {
+    float part = 0.f;
+    int row = 0, h = 0, ch = 0;
+    const bool live = w < n_work;
+    if (live) {
+      const int64_t rh = w / kTPR;
+      ch = (int)(w - rh * kTPR);
+      row = (int)(rh / H);
+      h = (int)(rh - (int64_t)row * H);
+      const uint4 a = *reinterpret_cast<const uint4*>(o + (int64_t)row * o_row_stride + (int64_t)h * DV + ch * 8);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + (int64_t)row * do_row_stride + (int64_t)h * DV + ch * 8);
+      part = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
+             bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
+             bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
+             bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
+    }
+#pragma unroll
+    for (int off = kTPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (live && ch == 0) {
+      int s, t;
+      S::locate(sh, tb, row, s, t);
+      const int64_t lbase = sh.varlen ? (int64_t)S::row0(sh, tb, s) : (int64_t)s * lse_seq_stride;
+      const float l = lse[(int64_t)h * lse_head_stride + lbase + t];
+      const int64_t g = ((int64_t)(S::tile_start(sh, tb, s) + t / kTile) * H + h) * kTile + (t % kTile);
+      ws.dsum[g] = part;
+      ws.lse2[g] = l * kLog2e;
+    }
+  }
+  // padding rows of each sequence's last q-tile: P must come out as zero there
+  for (int64_t w = tid; w < (int64_t)sh.nseq * H * kTile; w += nthreads) {
+    const int s = (int)(w / (H * kTile));
+    const int rem = (int)(w - (int64_t)s * H * kTile);
+    const int h = rem / kTile, r = rem % kTile;
+    const int L = S::length(sh, tb, s);
+    const int nt = cdiv(L, kTile);
+    if (nt == 0 || (nt - 1) * kTile + r < L) continue;
+    const int64_t g = ((int64_t)(S::tile_start(sh, tb, s) + nt - 1) * H + h) * kTile + r;
+    ws.dsum[g] = 0.f;
+    ws.lse2[g] = INFINITY;
+  }
+  // zero the dQ accumulator
+  float4* acc = reinterpret_cast<float4*>(ws.dq_acc);
+  const int64_t n4 = (int64_t)n_qtiles * H * kTile * DQK / 4;
+  for (int64_t i = tid; i < n4; i += nthreads) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+template <int DQK, int DV>
+struct BwdCfg {
+  static constexpr int kQPanels = DQK / 64;
+  static constexpr int kVPanels = DV / 64;
+  static constexpr int kKBytes = kQPanels * kPanelBytes;
+  static constexpr int kVBytes = kVPanels * kPanelBytes;
+  static constexpr int kQBytes = kQPanels * kPanelBytes;
+  static constexpr int kdOBytes = kVPanels * kPanelBytes;
+  static constexpr int kStatBytes = 2 * kTile * 4;  // lse2 + D of one q-tile
+  static constexpr int kStageBytes = kQBytes + kdOBytes + kStatBytes;
+  static constexpr int kPBytes = 2 * kPanelBytes;
+  static constexpr int kdSBytes = 2 * kPanelBytes;
+  static constexpr int kFixed = kKBytes + kVBytes + kPBytes + kdSBytes + 1024 + 1024;
+  static constexpr int kStagesFit = (kMaxSmem - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 3 ? 3 : kStagesFit;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kKBytes;
+  static constexpr int kOffP = kOffV + kVBytes;
+  static constexpr int kOffdS = kOffP + kPBytes;
+  static constexpr int kOffStage = kOffdS + kdSBytes;  // panels of every stage first
+  static constexpr int kOffStat = kOffStage + kStages * (kQBytes + kdOBytes);
+  static constexpr int kOffBar = kOffStat + kStages * kStatBytes;
+  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+  static_assert(kStages >= 1, "shared memory too small");
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
+  // Tensor memory plan (columns): see the file comment.
+  static constexpr bool kSharedSdP = (DQK == 192);  // S and dP take turns in one region
+  static constexpr bool kDqOnDp = (DQK == 128);     // dQ reuses the dP region
+  static constexpr uint32_t kTmemS = 0;
+  static constexpr uint32_t kTmemdP = kSharedSdP ? 0 : 128;
+  static constexpr uint32_t kTmemdV = kSharedSdP ? 192 : 256;
+  static constexpr uint32_t kTmemdK = kTmemdV + DV;
+  static constexpr uint32_t kTmemdQ = kSharedSdP ? 0 : (kDqOnDp ? 128 : kTmemdK + DQK);
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kTmemdK + DQK <= kTmemCols, "tensor memory budget (dK)");
+  static_assert(kTmemdQ + DQK <= kTmemCols, "tensor memory budget (dQ)");
+};
+
+struct BwdBars {
+  uint64_t item_full[2], item_empty[2];
+  uint64_t kv_full, kv_done, acc_free;
+  uint64_t q_full[3], q_empty[3];
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
+  uint64_t drain;
+  int item_slot[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct MainArgs {
+  int sem_bias;  // 0; a test sets it so that the ordered dQ wait can never succeed
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t dk_row_stride, dv_row_stride;
+  float scale, scale_log2;
+  int deterministic;
+  BwdWorkspace ws;
+  SeqShape sh;
+};
+
+template <int DQK, int DV, typename Tables>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const MainArgs a,
+                         const __grid_constant__ Tables tb) {
+  using C = BwdCfg<DQK, DV>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
+  const uint32_t sP = smem_u32(smem + C::kOffP);
+  const uint32_t sdS = smem_u32(smem + C::kOffdS);
+  const uint32_t sStage = smem_u32(smem + C::kOffStage);
+  const float* stat_f = reinterpret_cast<const float*>(smem + C::kOffStat);
+  const uint32_t sStat = smem_u32(smem + C::kOffStat);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SeqShape& sh = a.sh;
+  Abort ab{&bars->abort_flag, a.ws.header};
+
+  if (threadIdx.x == 0) {
+    bars->abort_flag = 0;
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&bars->item_full[k]), 1);
+      mbar_init(smem_u32(&bars->item_empty[k]), 1 + 8);  // MMA thread + 8 compute warps
+    }
+    mbar_init(smem_u32(&bars->kv_full), 1);
+    mbar_init(smem_u32(&bars->kv_done), 1);
+    mbar_init(smem_u32(&bars->acc_free), 8);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 1);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->p_full), 8);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->ds_full), 8);
+    mbar_init(smem_u32(&bars->dq_full), 1);
+    mbar_init(smem_u32(&bars->dq_free), 8);
+    mbar_init(smem_u32(&bars->drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ================================================= producer / claimer
+    if (lane == 0) {
+      uint32_t q_it = 0, kq = 0;
+      bool ok = true;
+      bool kv_issued = false;
+      for (uint32_t k = 0;; ++k) {
+        const uint32_t slot = k & 1;
+        if (!(ok = mbar_wait(smem_u32(&bars->item_empty[slot]), ((k >> 1) & 1) ^ 1, ab))) break;
+        // stop handing out work once any CTA has failed
+        const int item = ld_acquire_gpu(a.ws.header) != 0 ? sh.n_items
+                                                           : atomicAdd(&a.ws.header[1], 1);
+        bars->item_slot[slot] = item;
+        mbar_arrive(smem_u32(&bars->item_full[slot]));
+        if (item >= sh.n_items) break;
+        const Item it = decode_item(sh, tb, item, false);
+        const int krow0 = key_row0(sh, it);
+        // K_j, V_j once per item (the previous item's MMAs must be done with them)
+        if (!(ok = mbar_wait(smem_u32(&bars->kv_done), (k & 1) ^ 1, ab))) break;
+        const uint32_t kvb = smem_u32(&bars->kv_full);
+        mbar_arrive_expect_tx(kvb, C::kKBytes + C::kVBytes);
+        kv_issued = true;
+        kq = k;
+        for (int p = 0; p < C::kQPanels; ++p)
+          tma_load_3d(sK + p * kPanelBytes, &tm_k, kvb, p * 64, it.head, krow0 + it.tile * kTile);
+        for (int p = 0; p < C::kVPanels; ++p)
+          tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow0 + it.tile * kTile);
+        const int nq = cdiv(it.Lq, kTile);
+        const int i0 = sh.causal ? it.tile : 0;
+        for (int i = i0; i < nq; ++i, ++q_it) {
+          const uint32_t st = q_it % C::kStages;
+          if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), ((q_it / C::kStages) & 1) ^ 1, ab))) break;
+          const uint32_t qb = smem_u32(&bars->q_full[st]);
+          mbar_arrive_expect_tx(qb, C::kQBytes + C::kdOBytes + C::kStatBytes);
+          const uint32_t sQ = sStage + st * (C::kQBytes + C::kdOBytes);
+          const uint32_t sdO = sQ + C::kQBytes;
+          const int qrow = it.row0 + i * kTile;
+          for (int p = 0; p < C::kQPanels; ++p)
+            tma_load_3d(sQ + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
+          for (int p = 0; p < C::kVPanels; ++p)
+            tma_load_3d(sdO + p * kPanelBytes, &tm_do, qb, p * 64, it.head, qrow);
+          const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
+          bulk_load(sStat + st * C::kStatBytes, a.ws.lse2 + g * kTile, kTile * 4, qb);
+          bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.dsum + g * kTile, kTile * 4, qb);
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        if (kv_issued) mbar_wait_drain(smem_u32(&bars->kv_full), kq & 1);
+        const uint32_t first = q_it > (uint32_t)C::kStages ? q_it - C::kStages : 0;
+        for (uint32_t t = first; t < q_it; ++t)
+          mbar_wait_drain(smem_u32(&bars->q_full[t % C::kStages]), (t / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ================================================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
+      constexpr uint32_t idK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
+      constexpr uint32_t idQ = idesc_bf16(128, DQK, true, true);    // dQ = dS K
+      uint32_t q_it = 0, gi = 0;
+      bool ok = true;
+      for (uint32_t k = 0; ok; ++k) {
+        const uint32_t slot = k & 1;
+        if (!(ok = mbar_wait(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
+        const int item = bars->item_slot[slot];
+        if (item >= sh.n_items) break;
+        const Item it = decode_item(sh, tb, item, false);
+        const int nq = cdiv(it.Lq, kTile);
+        const int i0 = sh.causal ? it.tile : 0;
+        if (!(ok = mbar_wait(smem_u32(&bars->kv_full), k & 1, ab))) break;
+        // dK/dV accumulators of the previous item read out by the epilogue
+        if (!(ok = mbar_wait(smem_u32(&bars->acc_free), (k & 1) ^ 1, ab))) break;
+        tc_fence_after();
+        for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+          const uint32_t st = q_it % C::kStages;
+          const uint32_t sQ = sStage + st * (C::kQBytes + C::kdOBytes);
+          const uint32_t sdO = sQ + C::kQBytes;
+          const bool first = (i == i0);
+          if (!(ok = mbar_wait(smem_u32(&bars->q_full[st]), (q_it / C::kStages) & 1, ab))) break;
+          // S^T = K Q^T
+          if (C::kSharedSdP && gi > 0) {
+            if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            mma_bf16(tmem + C::kTmemS, desc_kmajor(sK, 128, kk), desc_kmajor(sQ, 128, kk), idS,
+                     kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&bars->s_full));
+          if (!C::kSharedSdP) {
+            // dP^T = V dO^T (its columns hold dQ of the previous step when aliased)
+            if (C::kDqOnDp && gi > 0) {
+              if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < DV / 16; ++kk)
+              mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO, 128, kk), idS,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&bars->dp_full));
+          }
+          // dV += P^T dO
+          if (!(ok = mbar_wait(smem_u32(&bars->p_full), gi & 1, ab))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16(tmem + C::kTmemdV, desc_kmajor(sP, 128, kk), desc_mnmajor(sdO, 128, kk), idV,
+                     (first && kk == 0) ? 0u : 1u);
+          if (C::kSharedSdP) {
+#pragma unroll
+            for (int kk = 0; kk < DV / 16; ++kk)
+              mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO, 128, kk), idS,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&bars->dp_full));
+          }
+          // dK += dS^T Q ; dQ = dS K
+          if (!(ok = mbar_wait(smem_u32(&bars->ds_full), gi & 1, ab))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16(tmem + C::kTmemdK, desc_kmajor(sdS, 128, kk), desc_mnmajor(sQ, 128, kk), idK,
+                     (first && kk == 0) ? 0u : 1u);
+          if (!C::kSharedSdP && !C::kDqOnDp && gi > 0) {
+            if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16(tmem + C::kTmemdQ, desc_mnmajor(sdS, 128, kk), desc_mnmajor(sK, 128, kk), idQ,
+                     kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&bars->dq_full));
+          mma_commit(smem_u32(&bars->q_empty[st]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->kv_done));
+        mbar_arrive(smem_u32(&bars->item_empty[slot]));
+      }
+      if (!ok) {
+        mma_commit(smem_u32(&bars->drain));
+        mbar_wait_drain(smem_u32(&bars->drain), 0);
+      }
+    }
+  } else {
+    // ================================================= compute warpgroups
+    const int grp = warp >> 2;                      // 0: columns 0-63, 1: columns 64-127
+    const int r = (warp & 3) * 32 + lane;           // TMEM lane: key row (S^T, dK, dV) or query row (dQ)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t q_it = 0, gi = 0;
+    bool ok = true;
+    for (uint32_t k = 0; ok; ++k) {
+      const uint32_t slot = k & 1;
+      if (!(ok = mbar_wait_warp(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
+      const int item = bars->item_slot[slot];
+      if (item >= sh.n_items) break;
+      const Item it = decode_item(sh, tb, item, false);
+      const int nq = cdiv(it.Lq, kTile);
+      const int nk = cdiv(it.Lk, kTile);
+      const int i0 = sh.causal ? it.tile : 0;
+      const int kidx = it.tile * kTile + r;  // this thread's key (S^T row)
+      const bool key_ok = kidx < it.Lk;
+      for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+        const uint32_t st = q_it % C::kStages;
+        const float* lse2 = stat_f + st * (C::kStatBytes / 4);
+        const float* dsum = lse2 + kTile;
+        // ---- P^T = exp2(S^T * s*log2e - LSE2)
+        if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
+        tc_fence_after();
+        uint32_t pr[2][32];
+        tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64, pr[0]);
+        tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64 + 32, pr[1]);
+        tmem_ld_wait();
+        const bool diag = sh.causal && (i == it.tile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const int q = grp * 64 + c * 32 + e;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float pe = ex2(__uint_as_float(pr[c][e + u]) * a.scale_log2 - lv[u]);
+              if (!key_ok || (diag && r > q + u)) pe = 0.f;
+              pr[c][e + u] = __float_as_uint(pe);
+            }
+          }
+        }
+        // P^T row (64 query columns) -> panel `grp` of sP
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int c = ch >> 2, e0 = (ch & 3) * 8;
+          st_shared_v4(sP + grp * kPanelBytes + sw128_offset(r, ch),
+                       pack_bf16(__uint_as_float(pr[c][e0 + 0]), __uint_as_float(pr[c][e0 + 1])),
+                       pack_bf16(__uint_as_float(pr[c][e0 + 2]), __uint_as_float(pr[c][e0 + 3])),
+                       pack_bf16(__uint_as_float(pr[c][e0 + 4]), __uint_as_float(pr[c][e0 + 5])),
+                       pack_bf16(__uint_as_float(pr[c][e0 + 6]), __uint_as_float(pr[c][e0 + 7])));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        // ---- dS^T = P^T ⊙ (dP^T − D)
+        if (!(ok = mbar_wait_warp(smem_u32(&bars->dp_full), gi & 1, ab))) break;
+        tc_fence_after();
+        uint32_t dr[2][32];
+        tmem_ld32(tmem + lane_base + C::kTmemdP + grp * 64, dr[0]);
+        tmem_ld32(tmem + lane_base + C::kTmemdP + grp * 64 + 32, dr[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const int q = grp * 64 + c * 32 + e;
+            const float4 d4 = *reinterpret_cast<const float4*>(dsum + q);
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dr[c][e + u] = __float_as_uint(__uint_as_float(pr[c][e + u]) *
+                                             (__uint_as_float(dr[c][e + u]) - dv4[u]));
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int c = ch >> 2, e0 = (ch & 3) * 8;
+          st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch),
+                       pack_bf16(__uint_as_float(dr[c][e0 + 0]), __uint_as_float(dr[c][e0 + 1])),
+                       pack_bf16(__uint_as_float(dr[c][e0 + 2]), __uint_as_float(dr[c][e0 + 3])),
+                       pack_bf16(__uint_as_float(dr[c][e0 + 4]), __uint_as_float(dr[c][e0 + 5])),
+                       pack_bf16(__uint_as_float(dr[c][e0 + 6]), __uint_as_float(dr[c][e0 + 7])));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
+        // ---- dQ_i partial (thread = query row r) -> fp32 accumulator
+        if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
+        tc_fence_after();
+        constexpr int kHalf = DQK / 2;  // 32, 64 or 96 columns per group
+        uint32_t qv[kHalf];
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c)
+          tmem_ld32(tmem + lane_base + C::kTmemdQ + grp * kHalf + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&qv[c * 32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+        const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
+        float* acc = a.ws.dq_acc + g * (kTile * DQK);
+        if (a.deterministic) {
+          // contributions to q-tile i are added in descending kv-tile order
+          int* sem = a.ws.sem + g;
+          const int target = (sh.causal ? (i - it.tile) : (nk - 1 - it.tile)) + a.sem_bias;
+          if (threadIdx.x == 0) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(sem) != target) {
+              // give up on our own limit, or as soon as any CTA has failed
+              if (ab.raised() || ld_acquire_gpu(a.ws.header) != 0 ||
+                  globaltimer() - t0 > kWaitLimitNs) {
+                ab.raise(kStatusTimeout);
+                break;
+              }
+            }
+          }
+          named_bar_sync(1, kComputeThreads);
+          if (ab.raised()) { ok = false; break; }
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < kHalf / 4; ++c4) {
+          const int col = grp * kHalf + c4 * 4;
+          red_add_v4(acc + ((col >> 2) * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+                     __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
+                     __uint_as_float(qv[c4 * 4 + 3]));
+        }
+        if (a.deterministic) {
+          named_bar_sync(1, kComputeThreads);
+          if (threadIdx.x == 0) {
+            __threadfence();
+            red_release_gpu_add(a.ws.sem + g, 1);
+          }
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: dK = s * acc, dV = acc (thread = key row r)
+      if (!(ok = mbar_wait_warp(smem_u32(&bars->kv_done), k & 1, ab))) break;
+      tc_fence_after();
+      const int krow = key_row0(sh, it) + kidx;
+#pragma unroll 1
+      for (int c = 0; c < DQK / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kTmemdK + grp * (DQK / 2) + c * 32, v);
+        tmem_ld_wait();
+        if (key_ok) {
+          __nv_bfloat16* dst = a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK +
+                               grp * (DQK / 2) + c * 32;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * a.scale, __uint_as_float(v[q4 * 8 + 1]) * a.scale);
+            w.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * a.scale, __uint_as_float(v[q4 * 8 + 3]) * a.scale);
+            w.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * a.scale, __uint_as_float(v[q4 * 8 + 5]) * a.scale);
+            w.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * a.scale, __uint_as_float(v[q4 * 8 + 7]) * a.scale);
+            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < DV / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kTmemdV + grp * (DV / 2) + c * 32, v);
+        tmem_ld_wait();
+        if (key_ok) {
+          __nv_bfloat16* dst = a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV +
+                               grp * (DV / 2) + c * 32;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]), __uint_as_float(v[q4 * 8 + 1]));
+            w.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]), __uint_as_float(v[q4 * 8 + 3]));
+            w.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]), __uint_as_float(v[q4 * 8 + 5]));
+            w.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]), __uint_as_float(v[q4 * 8 + 7]));
+            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars->acc_free));
+        mbar_arrive(smem_u32(&bars->item_empty[slot]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dQ conversion: one CTA per (q-tile, head)
+// ---------------------------------------------------------------------------
+template <int DQK, typename Tables>
+__global__ void __launch_bounds__(256)
+    attn_bwd_convert_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                            const int64_t dq_row_stride, const float scale, const SeqShape sh,
+                            const __grid_constant__ Tables tb) {
+  using S = SeqOf<Tables>;
+  extern __shared__ float tile_s[];  // [128][DQK + 4]
+  constexpr int kLd = DQK + 4;
+  const int g = blockIdx.x / sh.H;
+  const int h = blockIdx.x - g * sh.H;
+  int s, i;
+  S::tile_of(sh, tb, g, s, i);
+  const int L = S::length(sh, tb, s);
+  const int rows = min(kTile, L - i * kTile);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (int64_t)blockIdx.x * kTile * DQK);
+  for (int idx = threadIdx.x; idx < kTile * DQK / 4; idx += blockDim.x) {
+    const int c4 = idx / kTile, r = idx - c4 * kTile;
+    const float4 v = src[idx];
+    float* d = tile_s + r * kLd + c4 * 4;
+    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+  }
+  __syncthreads();
+  const int64_t row0 = S::row0(sh, tb, s) + (int64_t)i * kTile;
+  for (int idx = threadIdx.x; idx < rows * (DQK / 8); idx += blockDim.x) {
+    const int r = idx / (DQK / 8), c8 = idx - r * (DQK / 8);
+    const float* f = tile_s + r * kLd + c8 * 8;
+    uint4 w;
+    w.x = pack_bf16(f[0] * scale, f[1] * scale);
+    w.y = pack_bf16(f[2] * scale, f[3] * scale);
+    w.z = pack_bf16(f[4] * scale, f[5] * scale);
+    w.w = pack_bf16(f[6] * scale, f[7] * scale);
+    *reinterpret_cast<uint4*>(dq + (row0 + r) * dq_row_stride + (int64_t)h * DQK + c8 * 8) = w;
+  }
+}
+
+template <int DQK, int DV, typename Tables>
+cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
+  using C = BwdCfg<DQK, DV>;
+  const int total_rows = L.sh.varlen ? L.tables->cu[L.sh.nseq] : L.sh.nseq * L.sh.Tq;
+  // 1. preprocess
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.num_sms * 4);
+    cfg.blockDim = dim3(256);
+    cfg.stream = L.stream;
+    cudaError_t e = cudaLaunchKernelEx(
+        &cfg, attn_bwd_pre_kernel<DQK, DV, Tables>, reinterpret_cast<const __nv_bfloat16*>(L.o),
+        reinterpret_cast<const __nv_bfloat16*>(L.dout), L.lse, L.o_row_stride, L.do_row_stride,
+        L.lse_head_stride, L.lse_seq_stride, total_rows, L.n_qtiles, L.ws, L.sh, tb);
+    if (e != cudaSuccess) return e;
+  }
+  // 2. main
+  {
+    MainArgs a;
+    a.dk = reinterpret_cast<__nv_bfloat16*>(L.dk);
+    a.dv = reinterpret_cast<__nv_bfloat16*>(L.dv);
+    a.dk_row_stride = L.dk_row_stride;
+    a.dv_row_stride = L.dv_row_stride;
+    a.scale = L.scale;
+    a.scale_log2 = L.scale_log2;
+    a.deterministic = L.deterministic;
+    a.sem_bias = L.sem_bias;
+    a.ws = L.ws;
+    a.sh = L.sh;
+    auto* k = attn_bwd_main_kernel<DQK, DV, Tables>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid);
+    cfg.blockDim = dim3(kMainThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = L.stream;
+    e = cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, L.tm_do, a, tb);
+    if (e != cudaSuccess) return e;
+  }
+  // 3. dQ conversion
+  {
+    const int smem = kTile * (DQK + 4) * 4;
+    auto* k = attn_bwd_convert_kernel<DQK, Tables>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.n_qtiles * L.sh.H);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    e = cudaLaunchKernelEx(&cfg, k, static_cast<const float*>(L.ws.dq_acc),
+                           reinterpret_cast<__nv_bfloat16*>(L.dq), L.dq_row_stride, L.scale, L.sh, tb);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int DQK, int DV>
+cudaError_t launch_typed(const BwdLaunch& L) {
+  if (L.tables) return launch_all<DQK, DV, VarlenTables>(L, *L.tables);
+  return launch_all<DQK, DV, NoTables>(L, NoTables{});
+}
+
+}  // namespace
+
+int bwd_smem_bytes(int dqk, int dv) {
+  if (dqk == 64 && dv == 64) return BwdCfg<64, 64>::kSmemBytes;
+  if (dqk == 128 && dv == 128) return BwdCfg<128, 128>::kSmemBytes;
+  if (dqk == 192 && dv == 128) return BwdCfg<192, 128>::kSmemBytes;
+  return -1;
+}
+
+cudaError_t launch_bwd(const BwdLaunch& L, int dqk, int dv) {
+  if (dqk == 64 && dv == 64) return launch_typed<64, 64>(L);
+  if (dqk == 128 && dv == 128) return launch_typed<128, 128>(L);
+  if (dqk == 192 && dv == 128) return launch_typed<192, 128>(L);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,122 @@
+// attn_common.cuh — parameters and work decomposition shared by the forward
+// and backward kernels.
+//
+// Token rows.  Every input is viewed as rows of tokens: a fixed-length batch
+// (B, T, H, d) is the same memory as (B*T, H, d), and a variable-length batch
+// is (sum T, H, d) with sequence s occupying rows cu[s] .. cu[s+1]-1.  The
+// packed (B, T, 3, H, d) layout only changes the distance between rows.
+//
+// Tiles.  Queries and keys are cut into tiles of 128 consecutive rows of one
+// sequence and one head.  A q-tile is the unit of the forward and of the dQ
+// reduction; a kv-tile is the unit of the backward.  The last tile of a
+// sequence may be ragged; rows past the sequence end are masked.
+//
+// Work items and their order (the scheduling the first page describes in
+// §3.2 "确定性执行实现": CTA order swizzled over heads/batches for L2 reuse,
+// longest-processing-time-first over batches, and shortest-first over causal
+// kv-tiles for the deterministic dQ reduction):
+//   forward   item = (sequence, head, q-tile m): heads vary fastest so that
+//             concurrently running CTAs share K/V tiles in L2; q-tiles run
+//             from the longest causal row range down (m descending).
+//   backward  item = (sequence, head, kv-tile n): fast mode runs n ascending
+//             (the longest causal column range first); deterministic mode runs
+//             n descending, which is also the order in which each dQ tile
+//             receives its contributions, so a CTA only ever waits on work that
+//             was claimed before its own.
+//   Variable-length batches run sequence by sequence, longest first.
+#pragma once
+
+#include <stdint.h>
+
+namespace attn {
+
+constexpr int kTile = 128;
+constexpr int kMaxSeqs = 1024;  // sequences in one variable-length call
+
+// Host-computed tables for variable-length batches (passed by value).
+struct VarlenTables {
+  int cu[kMaxSeqs + 1];          // token offset of each sequence
+  int order[kMaxSeqs];           // sequences, longest first (ties: lower id first)
+  int item_start[kMaxSeqs + 1];  // first work item of the k-th sequence in `order`
+  int tile_start[kMaxSeqs + 1];  // first q-tile of sequence s in the workspace tile space
+};
+struct NoTables {};
+
+struct SeqShape {
+  int nseq;        // B (number of sequences)
+  int H;           // heads
+  int varlen;      // 1: lengths come from VarlenTables
+  int Tq, Tk;      // fixed-length sequence lengths (varlen: unused)
+  int nq_tiles;    // fixed-length: ceil(Tq/128)
+  int nk_tiles;    // fixed-length: ceil(Tk/128)
+  int n_items;     // number of work items of the kernel
+  int causal;
+  int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
+};
+
+struct Item {
+  int seq, head, tile;  // tile = q-tile (forward) or kv-tile (backward)
+  int row0;             // first token row of the sequence
+  int Lq, Lk;           // sequence lengths
+  int tile_base;        // first q-tile of this sequence in the workspace tile space
+};
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <typename Tables>
+__device__ __forceinline__ Item decode_item(const SeqShape& sh, const Tables& tb, int item,
+                                            bool forward);
+
+// Fixed length: rank = item / (B*H) picks the tile, the remainder the (b, h).
+template <>
+__device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const NoTables&,
+                                                      int item, bool forward) {
+  Item it;
+  const int bh = sh.nseq * sh.H;
+  const int rank = item / bh;
+  const int r = item - rank * bh;
+  it.seq = r / sh.H;
+  it.head = r - it.seq * sh.H;
+  if (forward) {
+    it.tile = sh.nq_tiles - 1 - rank;
+  } else {
+    it.tile = sh.descending ? sh.nk_tiles - 1 - rank : rank;
+  }
+  it.Lq = sh.Tq;
+  it.Lk = sh.Tk;
+  it.row0 = it.seq * sh.Tq;  // same for keys: fixed-length causal needs Tq == Tk,
+                             // non-causal keys use row0k below
+  it.tile_base = it.seq * sh.nq_tiles;
+  return it;
+}
+
+// Variable length: sequence-major in `order`, then tile rank, then head.
+template <>
+__device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
+                                                          const VarlenTables& tb, int item,
+                                                          bool forward) {
+  int lo = 0, hi = sh.nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb.item_start[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.seq = tb.order[lo];
+  const int local = item - tb.item_start[lo];
+  const int rank = local / sh.H;
+  it.head = local - rank * sh.H;
+  it.row0 = tb.cu[it.seq];
+  it.Lq = it.Lk = tb.cu[it.seq + 1] - it.row0;
+  const int nt = cdiv(it.Lq, kTile);
+  if (forward) it.tile = nt - 1 - rank;
+  else it.tile = sh.descending ? nt - 1 - rank : rank;
+  it.tile_base = tb.tile_start[it.seq];
+  return it;
+}
+
+// First token row of the keys of a sequence (fixed-length Tk may differ from Tq).
+__device__ __forceinline__ int key_row0(const SeqShape& sh, const Item& it) {
+  return sh.varlen ? it.row0 : it.seq * sh.Tk;
+}
+
+}  // namespace attn

@@ -1,0 +1,152 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) fused attention library
+ * (libattn_gb300.so).
+ *
+ * Operation.  Scaled-dot-product attention per (sequence, head):
+ *     S = s * Q K^T,  P = softmax(S) row by row,  O = P V,
+ * and its backward for the scalar loss whose gradient with respect to O is dO:
+ *     dV = P^T dO,  dP = dO V^T,  dS = P ⊙ (dP - D),  D_i = sum_k dO_ik O_ik,
+ *     dQ = s * dS K,  dK = s * dS^T Q.
+ * Defined in "ops(8)：self-attention 的 CUDA 实现及优化 (下) - 深度分析",
+ * §2.1 (forward, and the five backward steps with the softmax derivative) and
+ * Appendix A; D is the row sum of dP ⊙ P that the softmax backward subtracts
+ * (§2.1 step 3), computed from dO and O because the two are equal.  The
+ * forward also returns the softmax statistic the backward needs (§1.3 of the
+ * same page: "stats", only in training mode); here that is the natural-log
+ * log-sum-exp of the scaled scores, LSE_i = ln sum_j exp(S_ij).
+ * Causal masking: key j is visible to query i iff j <= i (the §2.2 CPU loop's
+ * t2 <= t), defined for Tq == Tk only.
+ *
+ * Precision.  Inputs and outputs are bf16; products accumulate in fp32; the
+ * softmax runs in fp32; P and dS are rounded to bf16 before they enter the
+ * tensor-core products; dQ is accumulated across key tiles in fp32.
+ *
+ * Memory.  Every pointer is a DEVICE pointer except `cu_seqlens` (host).
+ * The library allocates no device memory: the caller owns all buffers,
+ * including the backward workspace, sized with attn_bwd_workspace_size().
+ * Every tensor pointer must be 16-byte aligned.
+ *
+ * Layouts (`layout` argument):
+ *   ATTN_LAYOUT_BTHD (0): q (B,Tq,H,dqk), k (B,Tk,H,dqk), v (B,Tk,H,dv),
+ *       o and dO (B,Tq,H,dv); dq, dk, dv like q, k, v.
+ *   ATTN_LAYOUT_PACKED_QKV (1): q, k, v point at slots 0, 1, 2 of one
+ *       (B,T,3,H,d) buffer (k = q + H*d, v = q + 2*H*d elements), the format
+ *       of "ops(8)..." §1.3 (QKV as (B, T, 3, NH, HS), no permute); o and dO
+ *       are (B,T,H,d); dq, dk, dv likewise point at slots of a packed
+ *       (B,T,3,H,d) gradient buffer.  Needs dqk == dv and Tq == Tk.
+ *   Variable length: when `cu_seqlens` is non-NULL, B is the number of
+ *       sequences, Tq == Tk is the TOTAL number of token rows, tensors are
+ *       (Tq, H, d) (or (Tq, 3, H, d) packed), sequence b occupies rows
+ *       cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32, host memory, B+1 entries,
+ *       cu_seqlens[0] == 0, nondecreasing, cu_seqlens[B] == Tq), and LSE is
+ *       (H, Tq).  At most ATTN_MAX_VARLEN_SEQS sequences.
+ *   Fixed length: LSE is (B, H, Tq) fp32.
+ *
+ * Supported head sizes: (dqk, dv) in {(64, 64), (128, 128), (192, 128)}.
+ *
+ * Errors.  Functions return ATTN_OK (0) or a negative ATTN_ERR_* code.
+ * Argument errors are detected on the host before anything is launched.
+ * Launches are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream); a device-side failure (a bounded wait inside a kernel that
+ * gave up) is reported later through attn_fwd_status() / attn_bwd_status().
+ *
+ * Threading.  Calls on different streams with different workspaces may run
+ * concurrently.  Calls that share a workspace must be ordered on the GPU.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG (-1)         /* NULL / misaligned pointer, bad size */
+#define ATTN_ERR_UNSUPPORTED (-2)         /* head sizes, causal with Tq != Tk, ... */
+#define ATTN_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the query */
+#define ATTN_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
+#define ATTN_ERR_TIMEOUT (-5)             /* a kernel's bounded wait gave up */
+
+#define ATTN_LAYOUT_BTHD 0
+#define ATTN_LAYOUT_PACKED_QKV 1
+#define ATTN_MAX_VARLEN_SEQS 1024
+
+/*
+ * Forward: O and (unless lse == NULL, inference mode) LSE.
+ * q, k, v: inputs (bf16); o: output (bf16); lse: output (fp32) or NULL.
+ * B, H, Tq, Tk, dqk, dv: sizes (see Layouts); causal: 0/1; scale: the s in
+ * S = s Q K^T (the pages use 1/sqrt(dqk)); cu_seqlens: NULL or host offsets.
+ * "ops(8)..." §1.2-1.3 (sdpa returns [O, stats]; stats only when training),
+ * §2.1 forward formulas.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Tq, int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
+             int layout, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (varlen: 1 when
+ * cu_seqlens will be given; Tq is then the total token count).  The
+ * workspace holds the fp32 dQ accumulator, D and LSE*log2(e) per query row,
+ * one semaphore per (query tile, head), a work counter and a status word.
+ * Returns 0 for invalid sizes.  "ops(8)..." §1.3: the caller-provided
+ * workspace sized by a query, as the cuDNN graph does.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int dqk, int dv, int varlen,
+                               int deterministic);
+
+/*
+ * Backward: dq, dk, dv (bf16) from q, k, v, o, dO (bf16) and the forward's
+ * lse (fp32, required).  deterministic = 1 adds each key tile's dQ
+ * contribution in a fixed order (descending key tile, "深度学习反向传播优化：
+ * 2-CTA MMA模式与内存访问优化" §3.2), so results are bit-identical run to run;
+ * 0 uses unordered fp32 atomics (§3.1).  workspace: device memory of at least
+ * attn_bwd_workspace_size() bytes, 256-byte aligned; its contents need no
+ * initialisation.  "ops(8)..." §2.1 backward steps 1-5.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
+             int dqk, int dv, int causal, float scale, const int* cu_seqlens, int layout,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and returns the device status of the last backward
+ * that used `workspace` (ATTN_OK or ATTN_ERR_TIMEOUT).
+ */
+int attn_bwd_status(const void* workspace, void* stream);
+
+/*
+ * Synchronises `stream`, returns the sticky device status of the forward
+ * kernels on the current device (ATTN_OK or ATTN_ERR_TIMEOUT) and clears it.
+ */
+int attn_fwd_status(void* stream);
+
+/*
+ * Test hook (host-side fault injection; 0 = normal operation): every ordered
+ * dQ wait of later deterministic attn_bwd calls in this process waits for a
+ * semaphore value `bias` higher than the one that will come, so the bounded
+ * wait gives up and attn_bwd_status() reports ATTN_ERR_TIMEOUT.  The kernels
+ * stop, free their tensor memory and leave the CUDA context usable.  No
+ * counterpart on the pages (whose printed spin-wait, §3.2 of "深度学习反向传播
+ * 优化：2-CTA MMA模式与内存访问优化", has no bound).
+ */
+int attn_debug_set_wait_bias(int bias);
+
+/* Static text for an ATTN_* code. */
+const char* attn_strerror(int code);
+
+/*
+ * Host helper (no GPU needed): the order in which the kernels take the
+ * sequences of a variable-length batch — longest first, ties by index
+ * ("深度学习反向传播优化..." §3.2, batches sorted by expected time).
+ * Writes `nseq` sequence indices to order_out.  Returns ATTN_OK or
+ * ATTN_ERR_INVALID_ARG.
+ */
+int attn_varlen_order(const int* cu_seqlens, int nseq, int* order_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

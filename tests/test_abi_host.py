@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads and exports every symbol include/attn.h
+declares, and rejects bad arguments on the host before touching the GPU.
+No compute calls here (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from attention_backward_flashattention_gb300 import binding
+from attention_backward_flashattention_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A = 0x10000  # an aligned, never-dereferenced stand-in address
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return binding.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", src, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_strerror"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.EXPORTED) == set(names)
+
+
+def test_strerror(lib):
+    assert binding.attn_strerror(0) == "ok"
+    assert binding.attn_strerror(binding.ATTN_ERR_TIMEOUT) == "device wait timed out"
+    assert binding.attn_strerror(-99) == "unknown error"
+
+
+def _fwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Tq=128, Tk=128, dqk=64, dv=64, causal=1,
+                scale=0.125, cu_seqlens=None, layout=0, stream=0)
+    args.update(kw)
+    return binding.attn_fwd(**args)
+
+
+def _bwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, dq=A, dk=A, dv_out=A, B=1, H=2, Tq=128,
+                Tk=128, dqk=64, dv=64, causal=1, scale=0.125, cu_seqlens=None, layout=0,
+                deterministic=0, workspace=A, workspace_bytes=1 << 30, stream=0)
+    args.update(kw)
+    return binding.attn_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(o=A + 8), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lse=A + 2), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Tq=0, Tk=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(layout=7), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dqk=96, dv=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(dqk=128, dv=64), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(Tk=256), binding.ATTN_ERR_UNSUPPORTED),              # causal, Tq != Tk
+    (dict(layout=1, dqk=192, dv=128), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(cu_seqlens=[0, 100, 90], B=2, Tq=90, Tk=90), binding.ATTN_ERR_INVALID_ARG),
+    (dict(cu_seqlens=[0, 100, 200], B=2, Tq=300, Tk=300), binding.ATTN_ERR_INVALID_ARG),
+    (dict(cu_seqlens=[1, 100, 200], B=2, Tq=200, Tk=200), binding.ATTN_ERR_INVALID_ARG),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lse=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=A + 16), binding.ATTN_ERR_INVALID_ARG),   # must be 256-byte aligned
+    (dict(dq=A + 4), binding.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=1024), binding.ATTN_ERR_WORKSPACE_TOO_SMALL),
+    (dict(dqk=192, dv=192), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(causal=1, Tk=64), binding.ATTN_ERR_UNSUPPORTED),
+])
+def test_bwd_rejects(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_varlen_too_many_sequences(lib):
+    n = binding.MAX_VARLEN_SEQS + 1
+    cu = list(range(n + 1))
+    assert _fwd(cu_seqlens=cu, B=n, Tq=n, Tk=n) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_workspace_size_formula(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for (B, H, T, dqk, dv, varlen) in [(1, 16, 32768, 128, 128, 0), (8, 12, 1024, 64, 64, 0),
+                                       (2, 3, 200, 192, 128, 0), (40, 16, 32768, 128, 128, 1)]:
+        tiles = (-(-T // 128) + B) if varlen else B * -(-T // 128)
+        expect = (256 + r256(tiles * H * 4) + 2 * r256(tiles * H * 128 * 4)
+                  + r256(tiles * H * 128 * dqk * 4))
+        assert binding.attn_bwd_workspace_size(B, H, T, T, dqk, dv, varlen, 0) == expect
+    assert binding.attn_bwd_workspace_size(1, 1, 1, 1, 96, 96) == 0
+
+
+def test_varlen_order_longest_first(lib):
+    assert binding.attn_varlen_order([0, 5, 105, 106, 300]) == [3, 1, 0, 2]
+    # ties keep index order
+    assert binding.attn_varlen_order([0, 10, 20, 25, 35]) == [0, 1, 3, 2]
+    with pytest.raises(binding.AttnError):
+        binding.attn_varlen_order([0, 10, 5])
