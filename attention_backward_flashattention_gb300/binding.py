@@ -26,12 +26,14 @@ ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_WORKSPACE_TOO_SMALL = -3
 ATTN_ERR_CUDA = -4
 ATTN_ERR_TIMEOUT = -5
+ATTN_ERR_INTERNAL = -6
 LAYOUT_BTHD = 0
 LAYOUT_PACKED_QKV = 1
 MAX_VARLEN_SEQS = 1024
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
-            "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias")
+            "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
+            "attn_profile_main_kernel")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +72,8 @@ def load():
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_varlen_order.argtypes = [P, I, P]
         lib.attn_varlen_order.restype = I
+        lib.attn_profile_main_kernel.argtypes = [P, P]
+        lib.attn_profile_main_kernel.restype = I
         lib.attn_debug_set_wait_bias.argtypes = [I]
         lib.attn_debug_set_wait_bias.restype = I
         _lib = lib
@@ -149,6 +153,12 @@ def strerror(code: int) -> str:
         return attn_strerror(code)
     except RuntimeError:
         return f"code {code}"
+
+
+def attn_profile_main_kernel(event_start=None, event_stop=None) -> int:
+    """Record torch.cuda.Event (or raw cudaEvent_t) pairs around the backward main kernel."""
+    conv = lambda e: None if e is None else (e.cuda_event if hasattr(e, "cuda_event") else int(e))
+    return load().attn_profile_main_kernel(conv(event_start), conv(event_stop))
 
 
 def attn_debug_set_wait_bias(bias: int) -> int:

@@ -144,6 +144,11 @@ int cuda_err(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 // target of deterministic backward calls, so that the wait can never succeed.
 std::atomic<int> g_sem_bias{0};
 
+// Optional CUDA events recorded around the backward main kernel (benchmark
+// instrumentation; null = off).
+std::atomic<void*> g_prof_start{nullptr};
+std::atomic<void*> g_prof_stop{nullptr};
+
 }  // namespace
 
 extern "C" {
@@ -156,6 +161,7 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_INTERNAL: return "internal kernel set-up error";
     default: return "unknown error";
   }
 }
@@ -308,12 +314,21 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   L.n_qtiles = n_qtiles;
   L.deterministic = deterministic ? 1 : 0;
   L.sem_bias = g_sem_bias.load();
+  L.prof_start = static_cast<cudaEvent_t>(g_prof_start.load());
+  L.prof_stop = static_cast<cudaEvent_t>(g_prof_stop.load());
   const int sms = num_sms_current();
   if (sms <= 0) return ATTN_ERR_CUDA;
   L.num_sms = sms;
   L.grid = std::min(L.sh.n_items, sms);
   L.stream = static_cast<cudaStream_t>(stream);
   return cuda_err(launch_bwd(L, dqk, dv));
+}
+
+int attn_profile_main_kernel(void* event_start, void* event_stop) {
+  if ((event_start == nullptr) != (event_stop == nullptr)) return ATTN_ERR_INVALID_ARG;
+  g_prof_start.store(event_start);
+  g_prof_stop.store(event_stop);
+  return ATTN_OK;
 }
 
 int attn_debug_set_wait_bias(int bias) {

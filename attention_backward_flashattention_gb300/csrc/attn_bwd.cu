@@ -194,22 +194,25 @@ struct BwdCfg {
   static constexpr int kdOBytes = kVPanels * kPanelBytes;
   static constexpr int kStatBytes = 2 * kTile * 4;  // lse2 + D of one q-tile
   static constexpr int kStageBytes = kQBytes + kdOBytes + kStatBytes;
-  static constexpr int kPBytes = 2 * kPanelBytes;
   static constexpr int kdSBytes = 2 * kPanelBytes;
-  static constexpr int kFixed = kKBytes + kVBytes + kPBytes + kdSBytes + 1024 + 1024;
+  static constexpr int kBarBytes = 512;
+  // the dynamic shared memory window starts 1024-byte aligned (checked at run time)
+  static constexpr int kFixed = kKBytes + kVBytes + kdSBytes + kBarBytes;
   static constexpr int kStagesFit = (kMaxSmem - kFixed) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 3 ? 3 : kStagesFit;
+  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;  // barrier arrays hold 4
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKBytes;
-  static constexpr int kOffP = kOffV + kVBytes;
-  static constexpr int kOffdS = kOffP + kPBytes;
+  static constexpr int kOffdS = kOffV + kVBytes;
   static constexpr int kOffStage = kOffdS + kdSBytes;  // panels of every stage first
   static constexpr int kOffStat = kOffStage + kStages * (kQBytes + kdOBytes);
   static constexpr int kOffBar = kOffStat + kStages * kStatBytes;
-  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes;
   static_assert(kStages >= 1, "shared memory too small");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
-  // Tensor memory plan (columns): see the file comment.
+  static_assert(kBarBytes >= 256, "barrier block");
+  // Tensor memory plan (columns).  P^T (bf16, two per column) overwrites the
+  // S^T columns each warpgroup has already read: queries 0-63 at [0, 32),
+  // queries 64-127 at [64, 96).
   static constexpr bool kSharedSdP = (DQK == 192);  // S and dP take turns in one region
   static constexpr bool kDqOnDp = (DQK == 128);     // dQ reuses the dP region
   static constexpr uint32_t kTmemS = 0;
@@ -222,16 +225,23 @@ struct BwdCfg {
   static_assert(kTmemdQ + DQK <= kTmemCols, "tensor memory budget (dQ)");
 };
 
+// TMEM column of the packed P^T operand for MMA K-step kk (16 queries).
+__device__ __forceinline__ uint32_t p_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+constexpr int kMaxStages = 4;
+
 struct BwdBars {
   uint64_t item_full[2], item_empty[2];
   uint64_t kv_full, kv_done, acc_free;
-  uint64_t q_full[3], q_empty[3];
+  uint64_t q_full[kMaxStages], q_empty[kMaxStages];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
   uint64_t drain;
   int item_slot[2];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+static_assert(sizeof(BwdBars) <= 512, "barrier block size");
 
 struct MainArgs {
   int sem_bias;  // 0; a test sets it so that the ordered dQ wait can never succeed
@@ -252,13 +262,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                          const __grid_constant__ CUtensorMap tm_do, const MainArgs a,
                          const __grid_constant__ Tables tb) {
   using C = BwdCfg<DQK, DV>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the swizzled panels need a 1024-byte aligned window
+    if (threadIdx.x == 0) atomicCAS(a.ws.header, 0, kStatusInternal);
+    return;
+  }
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
   const uint32_t sK = smem_u32(smem + C::kOffK);
   const uint32_t sV = smem_u32(smem + C::kOffV);
-  const uint32_t sP = smem_u32(smem + C::kOffP);
   const uint32_t sdS = smem_u32(smem + C::kOffdS);
   const uint32_t sStage = smem_u32(smem + C::kOffStage);
   const float* stat_f = reinterpret_cast<const float*>(smem + C::kOffStat);
@@ -413,8 +424,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16(tmem + C::kTmemdV, desc_kmajor(sP, 128, kk), desc_mnmajor(sdO, 128, kk), idV,
-                     (first && kk == 0) ? 0u : 1u);
+            mma_bf16_ts(tmem + C::kTmemdV, tmem + C::kTmemS + p_col(kk),
+                        desc_mnmajor(sdO, 128, kk), idV, (first && kk == 0) ? 0u : 1u);
           if (C::kSharedSdP) {
 #pragma unroll
             for (int kk = 0; kk < DV / 16; ++kk)
@@ -494,17 +505,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
           }
         }
-        // P^T row (64 query columns) -> panel `grp` of sP
+        // P^T row (64 query columns, bf16 pairs) -> TMEM over the S^T columns
+        // this warpgroup has just read
+        {
+          uint32_t pk[32];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int c = ch >> 2, e0 = (ch & 3) * 8;
-          st_shared_v4(sP + grp * kPanelBytes + sw128_offset(r, ch),
-                       pack_bf16(__uint_as_float(pr[c][e0 + 0]), __uint_as_float(pr[c][e0 + 1])),
-                       pack_bf16(__uint_as_float(pr[c][e0 + 2]), __uint_as_float(pr[c][e0 + 3])),
-                       pack_bf16(__uint_as_float(pr[c][e0 + 4]), __uint_as_float(pr[c][e0 + 5])),
-                       pack_bf16(__uint_as_float(pr[c][e0 + 6]), __uint_as_float(pr[c][e0 + 7])));
+          for (int j = 0; j < 32; ++j)
+            pk[j] = pack_bf16(__uint_as_float(pr[j >> 4][(2 * j) & 31]),
+                              __uint_as_float(pr[j >> 4][(2 * j + 1) & 31]));
+          tmem_st32(tmem + lane_base + C::kTmemS + grp * 64, pk);
+          tmem_st_wait();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
@@ -724,8 +735,10 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     cfg.blockDim = dim3(kMainThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = L.stream;
+    if (L.prof_start && (e = cudaEventRecord(L.prof_start, L.stream)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, L.tm_do, a, tb);
     if (e != cudaSuccess) return e;
+    if (L.prof_stop && (e = cudaEventRecord(L.prof_stop, L.stream)) != cudaSuccess) return e;
   }
   // 3. dQ conversion
   {

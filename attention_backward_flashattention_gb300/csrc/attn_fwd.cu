@@ -58,6 +58,7 @@ struct FwdCfg {
   static constexpr uint32_t kTmemS = 0;
   static constexpr uint32_t kTmemO = 256;
   static_assert(kVStages >= 1, "shared memory too small");
+  static_assert(kKStages <= 4 && kVStages <= 4, "barrier arrays hold 4 stages");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 

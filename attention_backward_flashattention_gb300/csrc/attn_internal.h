@@ -53,6 +53,7 @@ struct BwdLaunch {
   int n_qtiles;       // q-tiles over all sequences (workspace tile space)
   int deterministic;
   int sem_bias;       // fault injection for tests (0 in normal use)
+  cudaEvent_t prof_start, prof_stop;  // recorded around the main kernel when set
   BwdWorkspace ws;
   SeqShape sh;        // n_items = kv-tile items
   const VarlenTables* tables;

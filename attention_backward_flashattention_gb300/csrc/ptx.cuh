@@ -22,6 +22,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // Error codes written to the device status word (mirrored by ATTN_ERR_* on the
 // host side).
 constexpr int kStatusTimeout = -5;
+constexpr int kStatusInternal = -6;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

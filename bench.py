@@ -1,0 +1,382 @@
+"""Benchmark: fused attention backward TFLOP/s on one GB300 (and N replicas).
+
+One step = the whole hot path on one batch of synthetic bf16 input: forward
+(O, LSE) then backward (preprocess, main kernel, dQ conversion), all through
+the C ABI.  The workload is causal, H=16, d=128, T=32768, B=1 (32K tokens).
+`value` = backward FLOPs 2*B*H*T^2*(3*dqk+2*dv)/2 / backward time, summed over
+ranks.  Inputs (5 x 134 MB) exceed the 126 MB L2, so no flush is needed
+between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm for this
+workload) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from attention_backward_flashattention_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "attn bwd TFLOP/s (bf16, causal, d=128, 32K tok) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = syn.HEADLINE
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_burst": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "hbm": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def _config(w, extra=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dqk": w.dqk, "dv": w.dv,
+         "causal": w.causal, "layout": "BTHD", "deterministic": w.deterministic,
+         "l2": "inputs larger than L2 (5 x 134 MB bf16), no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic_for(kernel_src, kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_name)
+    if not rec:
+        return None
+    with open(kernel_src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    if rec.get("source_sha256") != digest:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, rows_per_head, seed=0, x=None):
+    """Time the oracle's row-by-row backward on `rows_per_head` random query
+    rows of every head of `w` (one OpenMP thread per head).  Returns
+    (TFLOP/s in the metric's FLOP convention, seconds, threads, description)."""
+    import oracle
+    oracle.build()
+    if x is None:
+        x = syn.make_inputs(w)
+
+    def heads(t):
+        t = t.float().permute(0, 2, 1, 3).contiguous()
+        return list(t.reshape(-1, t.shape[2], t.shape[3]).double().numpy())
+
+    q, k, v, dO = (heads(x[n]) for n in ("q", "k", "v", "dO"))
+    rng = np.random.default_rng(seed)
+    rows = [np.sort(rng.choice(w.T, size=rows_per_head, replace=False)).astype(np.int32)
+            for _ in q]
+    per = 2.0 * (3 * w.dqk + 2 * w.dv)
+    flops = sum(per * ((r + 1).sum() if w.causal else w.T * len(r)) for r in rows)
+    t0 = time.perf_counter()
+    oracle.backward(q, k, v, dO, w.causal, w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle row-by-row backward (recomputes each row's forward), {rows_per_head} "
+            f"random query rows x {len(q)} heads of {w.name}; FLOPs counted as the rows' share "
+            f"of 2*H*T^2*(3*dqk+2*dv)/2")
+    return flops / dt / 1e12, dt, oracle.num_threads(), desc
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    from attention_backward_flashattention_gb300 import binding
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    x = syn.make_inputs(w)
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
+    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = binding.attn_bwd_workspace_size(B, H, T, T, dqk, dv, False, w.deterministic)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        rc = binding.attn_fwd(q, k, v, o, lse, B, H, T, T, dqk, dv, w.causal, w.scale, None, 0,
+                              stream)
+        assert rc == 0, rc
+
+    def bwd():
+        rc = binding.attn_bwd(q, k, v, o, dO, lse, dq, dk, dvv, B, H, T, T, dqk, dv, w.causal,
+                              w.scale, None, 0, w.deterministic, ws, need, stream)
+        assert rc == 0, rc
+
+    launches_per_step = 1 + 3
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if binding.attn_bwd_status(ws) != 0 or binding.attn_fwd_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for e in ev:       # create the events before the timed region
+        for z in e:
+            z.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        binding.attn_profile_main_kernel(e[3], e[4])
+        bwd()
+        e[2].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    binding.attn_profile_main_kernel(None, None)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    total_ms = t_start.elapsed_time(t_stop)
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    main_ms = [ev[i][3].elapsed_time(ev[i][4]) for i in range(K)]
+    if binding.attn_bwd_status(ws) != 0 or binding.attn_fwd_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    # e2e: pinned host inputs -> device, forward + backward, gradients -> host
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dO"))
+    hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dO.copy_(hdo, non_blocking=True)
+        fwd()
+        bwd()
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dvv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / K
+
+    stats = torch.tensor([total_ms, sum(bwd_ms), sum(fwd_ms), sum(main_ms), e2e_ms],
+                         dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
+    total_ms, bwd_sum, fwd_sum, main_sum, e2e_ms = stats.tolist()
+    if rank != 0:
+        return None
+
+    peaks = _peaks()
+    bwd_flops = w.bwd_flops()
+    fwd_flops = w.fwd_flops()
+    value = world * bwd_flops * K / (bwd_sum * 1e-3) / 1e12
+    main_avg_s = main_sum / K * 1e-3
+    achieved = bwd_flops / main_avg_s / 1e12
+    peak = peaks["bf16_sustained"]
+    traffic = _traffic_for(os.path.join(ROOT, "attention_backward_flashattention_gb300", "csrc",
+                                        "attn_bwd.cu"), "attn_bwd_main_kernel")
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, secs, cores, desc = oracle_sample(w, args.cpu_rows, x=x)
+        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 2)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, {"parallelism": f"replicas x{world} (independent heads, no exchange)"}),
+        "pct_of_bf16_peak": {"burst": 100.0 * value / world / peaks["bf16_burst"],
+                             "sustained": 100.0 * value / world / peaks["bf16_sustained"],
+                             "peaks": peaks["source"]},
+        "bwd_ms": bwd_sum / K, "fwd_ms": fwd_sum / K,
+        "fwd_tflops": world * fwd_flops * K / (fwd_sum * 1e-3) / 1e12,
+        "roofline": {"kernel": "attn_bwd_main_kernel", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": achieved / peaks["bf16_burst"],
+                     "traffic": traffic, "algorithmic_flops_per_launch": bwd_flops,
+                     "avg_launch_ms": main_avg_s * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * bwd_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = WORKLOAD
+    x = syn.make_inputs(w)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, max(4, rows // 8), seed=1000, x=x)
+    tfs, secs = [], []
+    desc, cores = "", 1
+    for s in range(args.steps):
+        tf, dt, cores, desc = oracle_sample(w, rows, seed=s, x=x)
+        tfs.append(tf)
+        secs.append(dt)
+    value = sum(tf * dt for tf, dt in zip(tfs, secs)) / sum(secs)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    global WORKLOAD
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--cpu-rows", type=int, default=384, help="oracle rows per head (cpu_baseline)")
+    ap.add_argument("--workload", default=syn.HEADLINE.name,
+                    help="fixed-length workload name (profiling runs on smaller cases)")
+    ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per head per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    WORKLOAD = syn.ALL[args.workload]
+    if WORKLOAD.varlen or WORKLOAD.layout != syn.LAYOUT_BTHD:
+        ap.error("bench workloads are fixed-length (B,T,H,d)")
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group(backend=backend)
+    if args.impl == "ours":
+        from attention_backward_flashattention_gb300 import build as build_mod
+        if rank == 0 or world == 1:
+            build_mod.build()
+        if world > 1:
+            torch.distributed.barrier()
+        line = run_ours(args, rank, world)
+    else:
+        line = run_reference(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -68,6 +68,7 @@ extern "C" {
 #define ATTN_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the query */
 #define ATTN_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
 #define ATTN_ERR_TIMEOUT (-5)             /* a kernel's bounded wait gave up */
+#define ATTN_ERR_INTERNAL (-6)            /* a kernel found its launch set-up unusable */
 
 #define ATTN_LAYOUT_BTHD 0
 #define ATTN_LAYOUT_PACKED_QKV 1
@@ -121,6 +122,16 @@ int attn_bwd_status(const void* workspace, void* stream);
  * kernels on the current device (ATTN_OK or ATTN_ERR_TIMEOUT) and clears it.
  */
 int attn_fwd_status(void* stream);
+
+/*
+ * Instrumentation: when both are non-NULL (cudaEvent_t handles), every later
+ * attn_bwd call records event_start on its stream just before the backward
+ * main kernel and event_stop just after it, so the caller can time that
+ * kernel alone.  Pass two NULLs to turn it off.  Returns ATTN_OK, or
+ * ATTN_ERR_INVALID_ARG when only one is NULL.  Benchmark support; no
+ * counterpart on the pages.
+ */
+int attn_profile_main_kernel(void* event_start, void* event_stop);
 
 /*
  * Test hook (host-side fault injection; 0 = normal operation): every ordered
