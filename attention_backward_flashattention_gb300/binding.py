@@ -27,13 +27,14 @@ ATTN_ERR_WORKSPACE_TOO_SMALL = -3
 ATTN_ERR_CUDA = -4
 ATTN_ERR_TIMEOUT = -5
 ATTN_ERR_INTERNAL = -6
+ATTN_ERR_SCRATCH_TOO_SMALL = -7
 LAYOUT_BTHD = 0
 LAYOUT_PACKED_QKV = 1
 MAX_VARLEN_SEQS = 1024
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
-            "attn_profile_main_kernel")
+            "attn_profile_main_kernel", "attn_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,9 @@ def load():
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P,
                                  SZ, P]
         lib.attn_bwd.restype = I
+        lib.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I,
+                                         I, P]
+        lib.attn_bwd_noalloc.restype = I
         lib.attn_bwd_status.argtypes = [P, P]
         lib.attn_bwd_status.restype = I
         lib.attn_fwd_status.argtypes = [P]
@@ -134,6 +138,17 @@ def attn_bwd(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
                            _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv, int(causal),
                            float(scale), cu.ptr, layout, int(deterministic), _ptr(workspace),
                            int(workspace_bytes), _stream(stream))
+
+
+def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal, scale,
+                     cu_seqlens=None, layout=LAYOUT_BTHD, deterministic=False,
+                     stream=None) -> int:
+    """attn_bwd without a caller workspace (the library's 32 MiB device array)."""
+    cu = _HostInts(cu_seqlens)
+    return load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv,
+                                   int(causal), float(scale), cu.ptr, layout, int(deterministic),
+                                   _stream(stream))
 
 
 def attn_bwd_status(workspace, stream=None) -> int:

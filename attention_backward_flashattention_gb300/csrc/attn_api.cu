@@ -162,6 +162,7 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
     case ATTN_ERR_INTERNAL: return "internal kernel set-up error";
+    case ATTN_ERR_SCRATCH_TOO_SMALL: return "problem needs more than the built-in 32 MiB scratch";
     default: return "unknown error";
   }
 }

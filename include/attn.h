@@ -69,6 +69,7 @@ extern "C" {
 #define ATTN_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
 #define ATTN_ERR_TIMEOUT (-5)             /* a kernel's bounded wait gave up */
 #define ATTN_ERR_INTERNAL (-6)            /* a kernel found its launch set-up unusable */
+#define ATTN_ERR_SCRATCH_TOO_SMALL (-7)   /* attn_bwd_noalloc: problem exceeds its scratch */
 
 #define ATTN_LAYOUT_BTHD 0
 #define ATTN_LAYOUT_PACKED_QKV 1
@@ -110,6 +111,25 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
              int dqk, int dv, int causal, float scale, const int* cu_seqlens, int layout,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward for callers that cannot allocate device memory (a plugin whose host
+ * framework owns all device memory, or a loop where a device-synchronising
+ * cudaMalloc is not allowed).  Same arguments and results as attn_bwd, minus
+ * the workspace: the library's own 32 MiB device array stands in for it, so
+ * it needs attn_bwd_workspace_size() <= 32 MiB (larger problems return
+ * ATTN_ERR_SCRATCH_TOO_SMALL; e.g. B=8, H=12, T=1024, d=64 fits).  The first
+ * call on each device looks up the array's address (make it before any stream
+ * capture); every device that loads this code holds the array until exit.
+ * All calls share the array: calls that overlap on the GPU race, so order
+ * them on one stream.  Device-side timeouts of these calls are not
+ * reported (there is no caller-visible workspace to read them from).  No
+ * counterpart on the pages.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq,
+                     int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
+                     int layout, int deterministic, void* stream);
 
 /*
  * Synchronises `stream` and returns the device status of the last backward
