@@ -29,12 +29,17 @@
 //      through an MN-major descriptor.
 //   3. attn_bwd_convert_kernel  dQ = bf16(s · dQacc) into the caller's layout.
 //
-// Roles in the main kernel (320 threads):
-//   warps 0-3, 4-7  compute warpgroups; thread = key row (TMEM lane); group g
-//                   handles query columns [64g, 64g+64) of S^T/dP^T and half
-//                   of the dQ / dK / dV columns in the reductions and epilogue
-//   warp 8          TMA producer and work-item claimer
-//   warp 9          MMA issuer, tensor-memory owner
+// Roles in the main kernel (512 threads):
+//   warps 0-3, 4-7  P / dS warpgroups; thread = key row (TMEM lane); group g
+//                   handles query columns [64g, 64g+64) of S^T and dP^T
+//   warps 8-11      dQ warpgroup: drains dQ_i from TMEM (thread = query row) and
+//                   adds it to the fp32 accumulator (ordered in deterministic
+//                   mode); at the end of an item stores dK and dV
+//   warp 12         TMA producer and work-item claimer
+//   warp 13         MMA issuer, tensor-memory owner (warps 14-15 idle)
+// MMA order per q-tile: ... dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, dV_{i+1} ...
+// so that P_{i+1} is computed while dK_i and dQ_i run (S and dP have their
+// own TMEM columns for d <= 128).
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -46,8 +51,24 @@ namespace {
 
 constexpr int kPanelBytes = kTile * 128;
 constexpr int kMaxSmem = 232448;
-constexpr int kMainThreads = 320;
-constexpr int kComputeThreads = 256;
+// 16 warps: P/dS warpgroups 0 and 1, dQ warpgroup 2, and warpgroup 3 whose
+// warp 12 is the TMA producer and warp 13 the MMA issuer (14, 15 idle).
+constexpr int kMainThreads = 512;
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+// Registers per thread after the split.  Launched with 512 x 128 = 65536;
+// the P/dS and control warpgroups give registers back, the dQ warpgroup (which
+// holds a whole dQ row of the tile) takes them.  Per warpgroup:
+//   P/dS x2, control, dQ    sum <= 4 x 128
+template <int DQK>
+struct RegSplit {
+  static constexpr uint32_t kLaunch = 128;
+  static constexpr uint32_t kCompute = DQK > 64 ? 104 : 112;
+  static constexpr uint32_t kCtl = DQK > 128 ? 88 : (DQK > 64 ? 120 : 96);
+  static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 192, 184, 216
+  static_assert(2 * kCompute + kCtl + kDq <= 4 * kLaunch, "register split");
+  static_assert(kCompute % 8 == 0 && kCtl % 8 == 0 && kDq % 8 == 0 && kDq <= 256, "setmaxnreg");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -233,14 +254,14 @@ constexpr int kMaxStages = 4;
 struct BwdBars {
   uint64_t item_full[2], item_empty[2];
   uint64_t kv_full, kv_done, acc_free;
-  uint64_t q_full[kMaxStages], q_empty[kMaxStages];
+  uint64_t q_full[kMaxStages], q_empty[kMaxStages];    // Q panels + LSE2 + D of a q-tile
+  uint64_t do_full[kMaxStages], do_empty[kMaxStages];  // dO panels
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
   uint64_t drain;
   int item_slot[2];
   uint32_t tmem_base;
   int abort_flag;
 };
-
 static_assert(sizeof(BwdBars) <= 512, "barrier block size");
 
 struct MainArgs {
@@ -278,34 +299,38 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int lane = threadIdx.x & 31;
   const SeqShape& sh = a.sh;
   Abort ab{&bars->abort_flag, a.ws.header};
+  auto sQ_of = [&](uint32_t st) { return sStage + st * (C::kQBytes + C::kdOBytes); };
+  auto sdO_of = [&](uint32_t st) { return sStage + st * (C::kQBytes + C::kdOBytes) + C::kQBytes; };
 
   if (threadIdx.x == 0) {
     bars->abort_flag = 0;
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&bars->item_full[k]), 1);
-      mbar_init(smem_u32(&bars->item_empty[k]), 1 + 8);  // MMA thread + 8 compute warps
+      mbar_init(smem_u32(&bars->item_empty[k]), 1 + 8 + 4);  // MMA + compute + dQ warps
     }
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_done), 1);
-    mbar_init(smem_u32(&bars->acc_free), 8);
+    mbar_init(smem_u32(&bars->acc_free), 4);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bars->q_full[s]), 1);
       mbar_init(smem_u32(&bars->q_empty[s]), 1);
+      mbar_init(smem_u32(&bars->do_full[s]), 1);
+      mbar_init(smem_u32(&bars->do_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->p_full), 8);
     mbar_init(smem_u32(&bars->dp_full), 1);
     mbar_init(smem_u32(&bars->ds_full), 8);
     mbar_init(smem_u32(&bars->dq_full), 1);
-    mbar_init(smem_u32(&bars->dq_free), 8);
+    mbar_init(smem_u32(&bars->dq_free), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kTmaWarp && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -316,12 +341,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 8) {
+  if (warp >= 12) {
+   regs_dec<RegSplit<DQK>::kCtl>();
+   if (warp == kTmaWarp && lane == 0) {
     // ================================================= producer / claimer
-    if (lane == 0) {
-      uint32_t q_it = 0, kq = 0;
-      bool ok = true;
-      bool kv_issued = false;
+    {
+      uint32_t q_it = 0, kq = 0, q_issued = 0;
+      bool ok = true, kv_issued = false;
       for (uint32_t k = 0;; ++k) {
         const uint32_t slot = k & 1;
         if (!(ok = mbar_wait(smem_u32(&bars->item_empty[slot]), ((k >> 1) & 1) ^ 1, ab))) break;
@@ -332,7 +358,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mbar_arrive(smem_u32(&bars->item_full[slot]));
         if (item >= sh.n_items) break;
         const Item it = decode_item(sh, tb, item, false);
-        const int krow0 = key_row0(sh, it);
+        const int krow = key_row0(sh, it) + it.tile * kTile;
         // K_j, V_j once per item (the previous item's MMAs must be done with them)
         if (!(ok = mbar_wait(smem_u32(&bars->kv_done), (k & 1) ^ 1, ab))) break;
         const uint32_t kvb = smem_u32(&bars->kv_full);
@@ -340,45 +366,88 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         kv_issued = true;
         kq = k;
         for (int p = 0; p < C::kQPanels; ++p)
-          tma_load_3d(sK + p * kPanelBytes, &tm_k, kvb, p * 64, it.head, krow0 + it.tile * kTile);
+          tma_load_3d(sK + p * kPanelBytes, &tm_k, kvb, p * 64, it.head, krow);
         for (int p = 0; p < C::kVPanels; ++p)
-          tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow0 + it.tile * kTile);
+          tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow);
         const int nq = cdiv(it.Lq, kTile);
         const int i0 = sh.causal ? it.tile : 0;
         for (int i = i0; i < nq; ++i, ++q_it) {
           const uint32_t st = q_it % C::kStages;
-          if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), ((q_it / C::kStages) & 1) ^ 1, ab))) break;
-          const uint32_t qb = smem_u32(&bars->q_full[st]);
-          mbar_arrive_expect_tx(qb, C::kQBytes + C::kdOBytes + C::kStatBytes);
-          const uint32_t sQ = sStage + st * (C::kQBytes + C::kdOBytes);
-          const uint32_t sdO = sQ + C::kQBytes;
+          const uint32_t par = ((q_it / C::kStages) & 1) ^ 1;
           const int qrow = it.row0 + i * kTile;
-          for (int p = 0; p < C::kQPanels; ++p)
-            tma_load_3d(sQ + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
-          for (int p = 0; p < C::kVPanels; ++p)
-            tma_load_3d(sdO + p * kPanelBytes, &tm_do, qb, p * 64, it.head, qrow);
           const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
+          if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), par, ab))) break;
+          const uint32_t qb = smem_u32(&bars->q_full[st]);
+          mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
+          for (int p = 0; p < C::kQPanels; ++p)
+            tma_load_3d(sQ_of(st) + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
           bulk_load(sStat + st * C::kStatBytes, a.ws.lse2 + g * kTile, kTile * 4, qb);
           bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.dsum + g * kTile, kTile * 4, qb);
+          q_issued = q_it + 1;
+          if (!(ok = mbar_wait(smem_u32(&bars->do_empty[st]), par, ab))) break;
+          const uint32_t db = smem_u32(&bars->do_full[st]);
+          mbar_arrive_expect_tx(db, C::kdOBytes);
+          for (int p = 0; p < C::kVPanels; ++p)
+            tma_load_3d(sdO_of(st) + p * kPanelBytes, &tm_do, db, p * 64, it.head, qrow);
         }
         if (!ok) break;
       }
       if (!ok) {
+        // let every copy already issued land before the CTA's memory is released
         if (kv_issued) mbar_wait_drain(smem_u32(&bars->kv_full), kq & 1);
-        const uint32_t first = q_it > (uint32_t)C::kStages ? q_it - C::kStages : 0;
-        for (uint32_t t = first; t < q_it; ++t)
+        for (uint32_t t = q_issued > (uint32_t)C::kStages ? q_issued - C::kStages : 0; t < q_issued; ++t)
           mbar_wait_drain(smem_u32(&bars->q_full[t % C::kStages]), (t / C::kStages) & 1);
+        for (uint32_t t = q_it > (uint32_t)C::kStages ? q_it - C::kStages : 0; t < q_it; ++t)
+          mbar_wait_drain(smem_u32(&bars->do_full[t % C::kStages]), (t / C::kStages) & 1);
       }
     }
-  } else if (warp == 9) {
+   } else if (warp == kMmaWarp && lane == 0) {
     // ================================================= MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
       constexpr uint32_t idK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
       constexpr uint32_t idQ = idesc_bf16(128, DQK, true, true);    // dQ = dS K
       uint32_t q_it = 0, gi = 0;
       bool ok = true;
+      auto W = [&](uint64_t& bar, uint32_t parity) -> bool {
+        if (!mbar_wait(smem_u32(&bar), parity, ab)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto mma_S = [&](uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_bf16(tmem + C::kTmemS, desc_kmajor(sK, 128, kk), desc_kmajor(sQ_of(st), 128, kk),
+                   idS, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars->s_full));
+      };
+      auto mma_dP = [&](uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO_of(st), 128, kk),
+                   idS, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars->dp_full));
+      };
+      auto mma_dV = [&](uint32_t st, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + C::kTmemdV, tmem + C::kTmemS + p_col(kk),
+                      desc_mnmajor(sdO_of(st), 128, kk), idV, (first && kk == 0) ? 0u : 1u);
+      };
+      auto mma_dK = [&](uint32_t st, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16(tmem + C::kTmemdK, desc_kmajor(sdS, 128, kk), desc_mnmajor(sQ_of(st), 128, kk),
+                   idK, (first && kk == 0) ? 0u : 1u);
+      };
+      auto mma_dQ = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16(tmem + C::kTmemdQ, desc_mnmajor(sdS, 128, kk), desc_mnmajor(sK, 128, kk), idQ,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars->dq_full));
+      };
       for (uint32_t k = 0; ok; ++k) {
         const uint32_t slot = k & 1;
         if (!(ok = mbar_wait(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
@@ -387,69 +456,60 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const Item it = decode_item(sh, tb, item, false);
         const int nq = cdiv(it.Lq, kTile);
         const int i0 = sh.causal ? it.tile : 0;
-        if (!(ok = mbar_wait(smem_u32(&bars->kv_full), k & 1, ab))) break;
+        if (!(ok = W(bars->kv_full, k & 1))) break;
         // dK/dV accumulators of the previous item read out by the epilogue
-        if (!(ok = mbar_wait(smem_u32(&bars->acc_free), (k & 1) ^ 1, ab))) break;
-        tc_fence_after();
-        for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
-          const uint32_t st = q_it % C::kStages;
-          const uint32_t sQ = sStage + st * (C::kQBytes + C::kdOBytes);
-          const uint32_t sdO = sQ + C::kQBytes;
-          const bool first = (i == i0);
-          if (!(ok = mbar_wait(smem_u32(&bars->q_full[st]), (q_it / C::kStages) & 1, ab))) break;
-          // S^T = K Q^T
-          if (C::kSharedSdP && gi > 0) {
-            if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            mma_bf16(tmem + C::kTmemS, desc_kmajor(sK, 128, kk), desc_kmajor(sQ, 128, kk), idS,
-                     kk > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&bars->s_full));
-          if (!C::kSharedSdP) {
-            // dP^T = V dO^T (its columns hold dQ of the previous step when aliased)
-            if (C::kDqOnDp && gi > 0) {
-              if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
-              tc_fence_after();
+        if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+        if (!C::kSharedSdP) {
+          // S and dP of the first q-tile; afterwards S_{i+1} is issued right
+          // after dV_i so that P_{i+1} is computed while dK_i and dQ_i run.
+          const uint32_t st0 = q_it % C::kStages;
+          if (!(ok = W(bars->q_full[st0], (q_it / C::kStages) & 1))) break;
+          mma_S(st0);
+          if (C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
+          if (!(ok = W(bars->do_full[st0], (q_it / C::kStages) & 1))) break;
+          mma_dP(st0);
+          for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+            const uint32_t st = q_it % C::kStages;
+            const uint32_t st1 = (q_it + 1) % C::kStages;
+            const uint32_t par1 = ((q_it + 1) / C::kStages) & 1;
+            const bool first = (i == i0), more = (i + 1 < nq);
+            if (!(ok = W(bars->p_full, gi & 1))) break;
+            mma_dV(st, first);
+            mma_commit(smem_u32(&bars->do_empty[st]));
+            if (more) {
+              if (!(ok = W(bars->q_full[st1], par1))) break;
+              mma_S(st1);
             }
-#pragma unroll
-            for (int kk = 0; kk < DV / 16; ++kk)
-              mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO, 128, kk), idS,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&bars->dp_full));
+            if (!(ok = W(bars->ds_full, gi & 1))) break;
+            mma_dK(st, first);
+            mma_commit(smem_u32(&bars->q_empty[st]));
+            if (!C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
+            mma_dQ();
+            if (more) {
+              if (C::kDqOnDp && !(ok = W(bars->dq_free, gi & 1))) break;
+              if (!(ok = W(bars->do_full[st1], par1))) break;
+              mma_dP(st1);
+            }
           }
-          // dV += P^T dO
-          if (!(ok = mbar_wait(smem_u32(&bars->p_full), gi & 1, ab))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ts(tmem + C::kTmemdV, tmem + C::kTmemS + p_col(kk),
-                        desc_mnmajor(sdO, 128, kk), idV, (first && kk == 0) ? 0u : 1u);
-          if (C::kSharedSdP) {
-#pragma unroll
-            for (int kk = 0; kk < DV / 16; ++kk)
-              mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO, 128, kk), idS,
-                       kk > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&bars->dp_full));
+        } else {
+          // S and dP share columns, and dQ covers them: one q-tile at a time
+          for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+            const uint32_t st = q_it % C::kStages;
+            const uint32_t par = (q_it / C::kStages) & 1;
+            const bool first = (i == i0);
+            if (!(ok = W(bars->q_full[st], par))) break;
+            if (gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
+            mma_S(st);
+            if (!(ok = W(bars->p_full, gi & 1))) break;
+            if (!(ok = W(bars->do_full[st], par))) break;
+            mma_dV(st, first);
+            mma_dP(st);  // overwrites the S/P columns after dV has read P
+            mma_commit(smem_u32(&bars->do_empty[st]));
+            if (!(ok = W(bars->ds_full, gi & 1))) break;
+            mma_dK(st, first);
+            mma_commit(smem_u32(&bars->q_empty[st]));
+            mma_dQ();
           }
-          // dK += dS^T Q ; dQ = dS K
-          if (!(ok = mbar_wait(smem_u32(&bars->ds_full), gi & 1, ab))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16(tmem + C::kTmemdK, desc_kmajor(sdS, 128, kk), desc_mnmajor(sQ, 128, kk), idK,
-                     (first && kk == 0) ? 0u : 1u);
-          if (!C::kSharedSdP && !C::kDqOnDp && gi > 0) {
-            if (!(ok = mbar_wait(smem_u32(&bars->dq_free), (gi - 1) & 1, ab))) break;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16(tmem + C::kTmemdQ, desc_mnmajor(sdS, 128, kk), desc_mnmajor(sK, 128, kk), idQ,
-                     kk > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&bars->dq_full));
-          mma_commit(smem_u32(&bars->q_empty[st]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&bars->kv_done));
@@ -460,10 +520,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mbar_wait_drain(smem_u32(&bars->drain), 0);
       }
     }
-  } else {
-    // ================================================= compute warpgroups
-    const int grp = warp >> 2;                      // 0: columns 0-63, 1: columns 64-127
-    const int r = (warp & 3) * 32 + lane;           // TMEM lane: key row (S^T, dK, dV) or query row (dQ)
+   }
+  } else if (warp < 8) {
+    regs_dec<RegSplit<DQK>::kCompute>();
+    // ================================================= P / dS warpgroups
+    const int grp = warp >> 2;                      // 0: queries 0-63, 1: queries 64-127
+    const int r = (warp & 3) * 32 + lane;           // TMEM lane = key row of S^T / dP^T
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t q_it = 0, gi = 0;
     bool ok = true;
@@ -474,92 +536,101 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (item >= sh.n_items) break;
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
-      const int nk = cdiv(it.Lk, kTile);
       const int i0 = sh.causal ? it.tile : 0;
-      const int kidx = it.tile * kTile + r;  // this thread's key (S^T row)
-      const bool key_ok = kidx < it.Lk;
+      const bool key_ok = it.tile * kTile + r < it.Lk;
       for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
         const uint32_t st = q_it % C::kStages;
-        const float* lse2 = stat_f + st * (C::kStatBytes / 4);
+        const float* lse2 = stat_f + st * (C::kStatBytes / 4) + grp * 64;
         const float* dsum = lse2 + kTile;
-        // ---- P^T = exp2(S^T * s*log2e - LSE2)
+        // ---- P^T = exp2(S^T * s*log2e - LSE2), masked; bf16 pairs -> TMEM
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
         tc_fence_after();
-        uint32_t pr[2][32];
-        tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64, pr[0]);
-        tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64 + 32, pr[1]);
-        tmem_ld_wait();
+        uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
         const bool diag = sh.causal && (i == it.tile);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64 + c * 32, sr);
+          tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const int q = grp * 64 + c * 32 + e;
+            const int q = c * 32 + e;  // query column within this group
             const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float pe[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              float pe = ex2(__uint_as_float(pr[c][e + u]) * a.scale_log2 - lv[u]);
-              if (!key_ok || (diag && r > q + u)) pe = 0.f;
-              pr[c][e + u] = __float_as_uint(pe);
+              pe[u] = ex2(__uint_as_float(sr[e + u]) * a.scale_log2 - lv[u]);
+              if (!key_ok || (diag && r > grp * 64 + q + u)) pe[u] = 0.f;
             }
+            pk[(q >> 1) + 0] = pack_bf16(pe[0], pe[1]);
+            pk[(q >> 1) + 1] = pack_bf16(pe[2], pe[3]);
           }
         }
-        // P^T row (64 query columns, bf16 pairs) -> TMEM over the S^T columns
-        // this warpgroup has just read
-        {
-          uint32_t pk[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pk[j] = pack_bf16(__uint_as_float(pr[j >> 4][(2 * j) & 31]),
-                              __uint_as_float(pr[j >> 4][(2 * j + 1) & 31]));
-          tmem_st32(tmem + lane_base + C::kTmemS + grp * 64, pk);
-          tmem_st_wait();
-        }
+        tmem_st32(tmem + lane_base + C::kTmemS + grp * 64, pk);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
-        // ---- dS^T = P^T ⊙ (dP^T − D)
+        // ---- dS^T = P^T ⊙ (dP^T − D) -> bf16 panel `grp` of sdS
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dp_full), gi & 1, ab))) break;
         tc_fence_after();
-        uint32_t dr[2][32];
-        tmem_ld32(tmem + lane_base + C::kTmemdP + grp * 64, dr[0]);
-        tmem_ld32(tmem + lane_base + C::kTmemdP + grp * 64 + 32, dr[1]);
-        tmem_ld_wait();
+        // the previous dS tile must have been consumed by its dK and dQ products
+        if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->dq_full), (gi - 1) & 1, ab))) break;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(tmem + lane_base + C::kTmemdP + grp * 64 + c * 32, dr);
+          tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int q = grp * 64 + c * 32 + e;
-            const float4 d4 = *reinterpret_cast<const float4*>(dsum + q);
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          for (int ch = 4 * c; ch < 4 * c + 4; ++ch) {
+            const int e0 = (ch & 3) * 8;
+            uint32_t w[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dr[c][e + u] = __float_as_uint(__uint_as_float(pr[c][e + u]) *
-                                             (__uint_as_float(dr[c][e + u]) - dv4[u]));
+            for (int u = 0; u < 4; ++u) {
+              const int q = ch * 8 + 2 * u;
+              const uint32_t pp = pk[q >> 1];
+              const float d0 = __uint_as_float(dr[e0 + 2 * u]) - dsum[q];
+              const float d1 = __uint_as_float(dr[e0 + 2 * u + 1]) - dsum[q + 1];
+              w[u] = pack_bf16(bf16_lo(pp) * d0, bf16_hi(pp) * d1);
+            }
+            st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch), w[0], w[1], w[2], w[3]);
           }
-        }
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int c = ch >> 2, e0 = (ch & 3) * 8;
-          st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch),
-                       pack_bf16(__uint_as_float(dr[c][e0 + 0]), __uint_as_float(dr[c][e0 + 1])),
-                       pack_bf16(__uint_as_float(dr[c][e0 + 2]), __uint_as_float(dr[c][e0 + 3])),
-                       pack_bf16(__uint_as_float(dr[c][e0 + 4]), __uint_as_float(dr[c][e0 + 5])),
-                       pack_bf16(__uint_as_float(dr[c][e0 + 6]), __uint_as_float(dr[c][e0 + 7])));
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
-        // ---- dQ_i partial (thread = query row r) -> fp32 accumulator
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->item_empty[slot]));
+    }
+  } else {
+    regs_inc<RegSplit<DQK>::kDq>();
+    // ================================================= dQ reduction + dK/dV epilogue
+    // warps 8-11: thread = TMEM lane = query row of dQ, key row of dK / dV
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int wt = threadIdx.x - 8 * 32;  // 0..127 within this warpgroup
+    uint32_t gi = 0;
+    bool ok = true;
+    for (uint32_t k = 0; ok; ++k) {
+      const uint32_t slot = k & 1;
+      if (!(ok = mbar_wait_warp(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
+      const int item = bars->item_slot[slot];
+      if (item >= sh.n_items) break;
+      const Item it = decode_item(sh, tb, item, false);
+      const int nq = cdiv(it.Lq, kTile);
+      const int nk = cdiv(it.Lk, kTile);
+      const int i0 = sh.causal ? it.tile : 0;
+      for (int i = i0; i < nq; ++i, ++gi) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
-        constexpr int kHalf = DQK / 2;  // 32, 64 or 96 columns per group
-        uint32_t qv[kHalf];
+        uint32_t qv[DQK];
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c)
-          tmem_ld32(tmem + lane_base + C::kTmemdQ + grp * kHalf + c * 32,
+        for (int c = 0; c < DQK / 32; ++c)
+          tmem_ld32(tmem + lane_base + C::kTmemdQ + c * 32,
                     *reinterpret_cast<uint32_t(*)[32]>(&qv[c * 32]));
         tmem_ld_wait();
         tc_fence_before();
@@ -571,7 +642,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           // contributions to q-tile i are added in descending kv-tile order
           int* sem = a.ws.sem + g;
           const int target = (sh.causal ? (i - it.tile) : (nk - 1 - it.tile)) + a.sem_bias;
-          if (threadIdx.x == 0) {
+          if (wt == 0) {
             const uint64_t t0 = globaltimer();
             while (ld_acquire_gpu(sem) != target) {
               // give up on our own limit, or as soon as any CTA has failed
@@ -582,19 +653,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
               }
             }
           }
-          named_bar_sync(1, kComputeThreads);
+          named_bar_sync(1, 128);
           if (ab.raised()) { ok = false; break; }
         }
 #pragma unroll
-        for (int c4 = 0; c4 < kHalf / 4; ++c4) {
-          const int col = grp * kHalf + c4 * 4;
-          red_add_v4(acc + ((col >> 2) * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+        for (int c4 = 0; c4 < DQK / 4; ++c4)
+          red_add_v4(acc + (c4 * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
                      __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
                      __uint_as_float(qv[c4 * 4 + 3]));
-        }
         if (a.deterministic) {
-          named_bar_sync(1, kComputeThreads);
-          if (threadIdx.x == 0) {
+          named_bar_sync(1, 128);
+          if (wt == 0) {
             __threadfence();
             red_release_gpu_add(a.ws.sem + g, 1);
           }
@@ -604,15 +673,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // ---- epilogue: dK = s * acc, dV = acc (thread = key row r)
       if (!(ok = mbar_wait_warp(smem_u32(&bars->kv_done), k & 1, ab))) break;
       tc_fence_after();
+      const int kidx = it.tile * kTile + r;
+      const bool key_ok = kidx < it.Lk;
       const int krow = key_row0(sh, it) + kidx;
 #pragma unroll 1
-      for (int c = 0; c < DQK / 64; ++c) {
+      for (int c = 0; c < DQK / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kTmemdK + grp * (DQK / 2) + c * 32, v);
+        tmem_ld32(tmem + lane_base + C::kTmemdK + c * 32, v);
         tmem_ld_wait();
         if (key_ok) {
-          __nv_bfloat16* dst = a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK +
-                               grp * (DQK / 2) + c * 32;
+          __nv_bfloat16* dst = a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK + c * 32;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -625,13 +695,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int c = 0; c < DV / 64; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kTmemdV + grp * (DV / 2) + c * 32, v);
+        tmem_ld32(tmem + lane_base + C::kTmemdV + c * 32, v);
         tmem_ld_wait();
         if (key_ok) {
-          __nv_bfloat16* dst = a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV +
-                               grp * (DV / 2) + c * 32;
+          __nv_bfloat16* dst = a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV + c * 32;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -654,7 +723,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
