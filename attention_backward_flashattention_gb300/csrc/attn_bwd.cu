@@ -21,7 +21,8 @@
 //         P^T  = exp2(S^T·s·log2e − LSE2_i)   (compute warps)
 //         dP^T = V_j dO_i^T                   (MMA, TMEM)
 //         dV_j += P^T dO_i                    (MMA)
-//         dS^T = P^T ⊙ (dP^T − D_i)           (compute warps, bf16 to smem)
+//         dS^T = P^T ⊙ (dP^T − D_i)           (compute warps, bf16 to smem;
+//                                               dP^T − D rounded to bf16 first)
 //         dK_j += dS^T Q_i                    (MMA)
 //         dQ_i  = dS K_j                      (MMA, TMEM) -> fp32 reduction
 //      Working transposed (keys on TMEM lanes) makes P^T and dS^T the natural
@@ -585,14 +586,19 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
           for (int ch = 4 * c; ch < 4 * c + 4; ++ch) {
             const int e0 = (ch & 3) * 8;
+            const float4 da = *reinterpret_cast<const float4*>(dsum + ch * 8);
+            const float4 db = *reinterpret_cast<const float4*>(dsum + ch * 8 + 4);
+            const float dv8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+            // dS = P * (dP - D): the difference in fp32, rounded to bf16, then
+            // multiplied by the bf16 P pair (the product is rounded to bf16 for
+            // the MMAs anyway)
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int q = ch * 8 + 2 * u;
-              const uint32_t pp = pk[q >> 1];
-              const float d0 = __uint_as_float(dr[e0 + 2 * u]) - dsum[q];
-              const float d1 = __uint_as_float(dr[e0 + 2 * u + 1]) - dsum[q + 1];
-              w[u] = pack_bf16(bf16_lo(pp) * d0, bf16_hi(pp) * d1);
+              const uint32_t pp = pk[ch * 4 + u];
+              const float d0 = __uint_as_float(dr[e0 + 2 * u]) - dv8[2 * u];
+              const float d1 = __uint_as_float(dr[e0 + 2 * u + 1]) - dv8[2 * u + 1];
+              w[u] = mul_bf16x2(pp, pack_bf16(d0, d1));
             }
             st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch), w[0], w[1], w[2], w[3]);
           }

@@ -15,14 +15,16 @@
 // §3.2 "确定性执行实现": CTA order swizzled over heads/batches for L2 reuse,
 // longest-processing-time-first over batches, and shortest-first over causal
 // kv-tiles for the deterministic dQ reduction):
-//   forward   item = (sequence, head, q-tile m): heads vary fastest so that
-//             concurrently running CTAs share K/V tiles in L2; q-tiles run
-//             from the longest causal row range down (m descending).
-//   backward  item = (sequence, head, kv-tile n): fast mode runs n ascending
-//             (the longest causal column range first); deterministic mode runs
-//             n descending, which is also the order in which each dQ tile
-//             receives its contributions, so a CTA only ever waits on work that
-//             was claimed before its own.
+//   forward   item = (sequence, head, q-tile m), taken by a static round-robin
+//             over CTAs: q-tiles longest causal row range first (m descending)
+//             with heads varying fastest, which keeps the round-robin balanced.
+//   backward  item = (sequence, head, kv-tile n); all tiles of one (sequence,
+//             head) are consecutive, so one head's Q, dO and fp32 dQ
+//             accumulator stay in L2 while ~one SM count of its kv-tiles run.
+//             Fast mode runs n ascending (the longest causal column range
+//             first); deterministic mode runs n descending, which is also the
+//             order in which each dQ tile receives its contributions, so a CTA
+//             only ever waits on work that was claimed before its own.
 //   Variable-length batches run sequence by sequence, longest first.
 #pragma once
 
@@ -67,21 +69,26 @@ template <typename Tables>
 __device__ __forceinline__ Item decode_item(const SeqShape& sh, const Tables& tb, int item,
                                             bool forward);
 
-// Fixed length: rank = item / (B*H) picks the tile, the remainder the (b, h).
+// Fixed length.  Forward: item / (B*H) is the q-tile's rank (longest first) and
+// the remainder the (b, h), so a static round-robin over CTAs stays balanced.
+// Backward (claimed dynamically): item / (kv-tiles per head) is the (b, h).
 template <>
 __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const NoTables&,
                                                       int item, bool forward) {
   Item it;
-  const int bh = sh.nseq * sh.H;
-  const int rank = item / bh;
-  const int r = item - rank * bh;
-  it.seq = r / sh.H;
-  it.head = r - it.seq * sh.H;
-  if (forward) {
+  int bh, rank;
+  if (forward) {  // tile rank major, (b, h) fastest
+    const int nbh = sh.nseq * sh.H;
+    rank = item / nbh;
+    bh = item - rank * nbh;
     it.tile = sh.nq_tiles - 1 - rank;
-  } else {
+  } else {        // (b, h) major, tile rank fastest
+    bh = item / sh.nk_tiles;
+    rank = item - bh * sh.nk_tiles;
     it.tile = sh.descending ? sh.nk_tiles - 1 - rank : rank;
   }
+  it.seq = bh / sh.H;
+  it.head = bh - it.seq * sh.H;
   it.Lq = sh.Tq;
   it.Lk = sh.Tk;
   it.row0 = it.seq * sh.Tq;  // same for keys: fixed-length causal needs Tq == Tk,
@@ -90,7 +97,7 @@ __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const 
   return it;
 }
 
-// Variable length: sequence-major in `order`, then tile rank, then head.
+// Variable length: sequence-major in `order`; within a sequence as above.
 template <>
 __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
                                                           const VarlenTables& tb, int item,
@@ -103,11 +110,17 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   Item it;
   it.seq = tb.order[lo];
   const int local = item - tb.item_start[lo];
-  const int rank = local / sh.H;
-  it.head = local - rank * sh.H;
   it.row0 = tb.cu[it.seq];
   it.Lq = it.Lk = tb.cu[it.seq + 1] - it.row0;
   const int nt = cdiv(it.Lq, kTile);
+  int rank;
+  if (forward) {  // tile rank, then head
+    rank = local / sh.H;
+    it.head = local - rank * sh.H;
+  } else {        // head, then tile rank
+    it.head = local / nt;
+    rank = local - it.head * nt;
+  }
   if (forward) it.tile = nt - 1 - rank;
   else it.tile = sh.descending ? nt - 1 - rank : rank;
   it.tile_base = tb.tile_start[it.seq];
