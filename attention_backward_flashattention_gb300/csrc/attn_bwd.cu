@@ -64,9 +64,9 @@ constexpr int kMmaWarp = 13;
 template <int DQK>
 struct RegSplit {
   static constexpr uint32_t kLaunch = 128;
-  static constexpr uint32_t kCompute = DQK > 64 ? 104 : 112;
-  static constexpr uint32_t kCtl = DQK > 128 ? 88 : (DQK > 64 ? 120 : 96);
-  static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 192, 184, 216
+  static constexpr uint32_t kCompute = DQK > 128 ? 96 : (DQK > 64 ? 104 : 112);
+  static constexpr uint32_t kCtl = DQK > 128 ? 112 : (DQK > 64 ? 128 : 112);
+  static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 176, 176, 208
   static_assert(2 * kCompute + kCtl + kDq <= 4 * kLaunch, "register split");
   static_assert(kCompute % 8 == 0 && kCtl % 8 == 0 && kDq % 8 == 0 && kDq <= 256, "setmaxnreg");
 };
@@ -416,36 +416,47 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_after();
         return true;
       };
+      // Descriptor bases: fixed buffers once, staged buffers per call; each
+      // MMA then only adds a constant (see kmajor_step / mnmajor_step).
+      const uint64_t bK_k = kmajor_base(sK), bK_mn = mnmajor_base(sK, 128);
+      const uint64_t bV_k = kmajor_base(sV);
+      const uint64_t bdS_k = kmajor_base(sdS), bdS_mn = mnmajor_base(sdS, 128);
+      const uint32_t tS = tmem + C::kTmemS, tdP = tmem + C::kTmemdP;
+      const uint32_t tdV = tmem + C::kTmemdV, tdK = tmem + C::kTmemdK, tdQ = tmem + C::kTmemdQ;
       auto mma_S = [&](uint32_t st) {
+        const uint64_t bQ = kmajor_base(sQ_of(st));
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
-          mma_bf16(tmem + C::kTmemS, desc_kmajor(sK, 128, kk), desc_kmajor(sQ_of(st), 128, kk),
-                   idS, kk > 0 ? 1u : 0u);
+          mma_bf16(tS, bK_k + kmajor_step(kk, 128), bQ + kmajor_step(kk, 128), idS,
+                   kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&bars->s_full));
       };
       auto mma_dP = [&](uint32_t st) {
+        const uint64_t bdO = kmajor_base(sdO_of(st));
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          mma_bf16(tmem + C::kTmemdP, desc_kmajor(sV, 128, kk), desc_kmajor(sdO_of(st), 128, kk),
-                   idS, kk > 0 ? 1u : 0u);
+          mma_bf16(tdP, bV_k + kmajor_step(kk, 128), bdO + kmajor_step(kk, 128), idS,
+                   kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&bars->dp_full));
       };
       auto mma_dV = [&](uint32_t st, bool first) {
+        const uint64_t bdO = mnmajor_base(sdO_of(st), 128);
+        mma_bf16_ts(tdV, tS + p_col(0), bdO, idV, first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + C::kTmemdV, tmem + C::kTmemS + p_col(kk),
-                      desc_mnmajor(sdO_of(st), 128, kk), idV, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 1; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tdV, tS + p_col(kk), bdO + mnmajor_step(kk), idV, 1u);
       };
       auto mma_dK = [&](uint32_t st, bool first) {
+        const uint64_t bQ = mnmajor_base(sQ_of(st), 128);
+        mma_bf16(tdK, bdS_k, bQ, idK, first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16(tmem + C::kTmemdK, desc_kmajor(sdS, 128, kk), desc_mnmajor(sQ_of(st), 128, kk),
-                   idK, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 1; kk < kTile / 16; ++kk)
+          mma_bf16(tdK, bdS_k + kmajor_step(kk, 128), bQ + mnmajor_step(kk), idK, 1u);
       };
       auto mma_dQ = [&]() {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16(tmem + C::kTmemdQ, desc_mnmajor(sdS, 128, kk), desc_mnmajor(sK, 128, kk), idQ,
+          mma_bf16(tdQ, bdS_mn + mnmajor_step(kk), bK_mn + mnmajor_step(kk), idQ,
                    kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&bars->dq_full));
       };

@@ -182,16 +182,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idO = idesc_bf16(128, DV, false, true);
       uint32_t kv_it = 0, sc = 0, item_iter = 0;
       bool ok = true;
+      // descriptor bases (each MMA then only adds a constant)
+      const uint64_t bQ_k = kmajor_base(sQ), bP_k = kmajor_base(sP);
+      const uint32_t tO = tmem + C::kTmemO;
       auto issue_pv = [&](uint32_t t_kv, uint32_t t_s, bool first) -> bool {
         if (!mbar_wait(smem_u32(&bars->p_full), t_s & 1, ab)) return false;
         tc_fence_after();
         const uint32_t sv = t_kv % C::kVStages;
         if (!mbar_wait(smem_u32(&bars->v_full[sv]), (t_kv / C::kVStages) & 1, ab)) return false;
-        const uint32_t vb = sV + sv * C::kVBytes;
+        const uint64_t bV = mnmajor_base(sV + sv * C::kVBytes, 128);
+        mma_bf16(tO, bP_k, bV, idO, first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16(tmem + C::kTmemO, desc_kmajor(sP, 128, kk), desc_mnmajor(vb, 128, kk), idO,
-                   (first && kk == 0) ? 0u : 1u);
+        for (int kk = 1; kk < kTile / 16; ++kk)
+          mma_bf16(tO, bP_k + kmajor_step(kk, 128), bV + mnmajor_step(kk), idO, 1u);
         mma_commit(smem_u32(&bars->o_done));
         mma_commit(smem_u32(&bars->v_empty[sv]));
         return true;
@@ -210,11 +213,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!(ok = mbar_wait(smem_u32(&bars->k_full[sk]), (t / C::kKStages) & 1, ab))) break;
           if (!(ok = mbar_wait(smem_u32(&bars->s_free[b]), ((ts >> 1) & 1) ^ 1, ab))) break;
           tc_fence_after();
-          const uint32_t kb = sK + sk * C::kKBytes;
+          const uint64_t bK = kmajor_base(sK + sk * C::kKBytes);
+          const uint32_t tS = tmem + C::kTmemS + b * 128;
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk)
-            mma_bf16(tmem + C::kTmemS + b * 128, desc_kmajor(sQ, 128, kk),
-                     desc_kmajor(kb, 128, kk), idS, kk > 0 ? 1u : 0u);
+            mma_bf16(tS, bQ_k + kmajor_step(kk, 128), bK + kmajor_step(kk, 128), idS,
+                     kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&bars->s_full[b]));
           mma_commit(smem_u32(&bars->k_empty[sk]));
           if (j == nkv - 1) mma_commit(smem_u32(&bars->q_empty));

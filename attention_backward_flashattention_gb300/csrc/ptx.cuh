@@ -294,6 +294,26 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, uint32_t rows, u
   return sdesc_sw128(tile + kk * 2048u, panel_bytes, 1024u);
 }
 
+// The same descriptors split into a base (computed once per buffer) and a
+// per-K-step increment (a compile-time constant once the K loop is unrolled):
+// desc_kmajor(t, rows, kk) == kmajor_base(t) + kmajor_step(kk, rows), and
+// likewise for MN-major.  The increment only touches the start-address field,
+// which cannot carry because shared-memory addresses stay below 256 KB.  The
+// MMA-issuing thread must keep up with one MMA every 64 cycles, so it should
+// do no more than an add per instruction.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
+  return sdesc_sw128(tile, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t mnmajor_base(uint32_t tile, uint32_t rows) {
+  return sdesc_sw128(tile, rows * 128u, 1024u);
+}
+__host__ __device__ constexpr uint64_t kmajor_step(int kk, uint32_t rows) {
+  return (uint64_t)(((uint32_t)(kk >> 2) * rows * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 // Bits: D format 4-5 (1 = f32), A format 7-9 (1 = bf16), B format 10-12,
 // A major 15 / B major 16 (1 = MN-major), N >> 3 in 17-22, M >> 4 in 24-28.
