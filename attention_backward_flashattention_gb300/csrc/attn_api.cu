@@ -77,7 +77,8 @@ int order_impl(const int* cu, int nseq, int* order) {
 
 // Variable-length tables: sequences longest first; items per sequence are
 // (tiles of that sequence) x H; q-tiles numbered sequence by sequence.
-void build_tables(const int* cu, int nseq, int H, VarlenTables* t, int* n_items, int* n_qtiles) {
+void build_tables(const int* cu, int nseq, int H, int unit_rows, VarlenTables* t, int* n_items,
+                  int* n_qtiles) {
   std::memset(t, 0, sizeof(*t));
   for (int b = 0; b <= nseq; ++b) t->cu[b] = cu[b];
   order_impl(cu, nseq, t->order);
@@ -85,7 +86,7 @@ void build_tables(const int* cu, int nseq, int H, VarlenTables* t, int* n_items,
   for (int k = 0; k < nseq; ++k) {
     t->item_start[k] = acc;
     const int s = t->order[k];
-    acc += cdiv(cu[s + 1] - cu[s], kTile) * H;
+    acc += cdiv(cu[s + 1] - cu[s], unit_rows) * H;
   }
   t->item_start[nseq] = acc;
   *n_items = acc;
@@ -207,17 +208,18 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   L.sh.Tk = Tk;
   L.sh.nq_tiles = cdiv(Tq, kTile);
   L.sh.nk_tiles = cdiv(Tk, kTile);
+  L.sh.nq_units = cdiv(Tq, kFwdRows);
   L.sh.causal = causal ? 1 : 0;
   L.sh.descending = 0;
   if (varlen) {
     int n_items = 0, n_qt = 0;
-    build_tables(cu_seqlens, B, H, &tables, &n_items, &n_qt);
+    build_tables(cu_seqlens, B, H, kFwdRows, &tables, &n_items, &n_qt);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
     L.lse_seq_stride = 0;
   } else {
-    L.sh.n_items = B * H * L.sh.nq_tiles;
+    L.sh.n_items = B * H * L.sh.nq_units;
     L.tables = nullptr;
     L.lse_head_stride = Tq;
     L.lse_seq_stride = (int64_t)H * Tq;
@@ -275,7 +277,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   int n_qtiles;
   if (varlen) {
     int n_items = 0;
-    build_tables(cu_seqlens, B, H, &tables, &n_items, &n_qtiles);
+    build_tables(cu_seqlens, B, H, kTile, &tables, &n_items, &n_qtiles);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;

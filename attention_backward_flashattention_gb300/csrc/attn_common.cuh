@@ -15,9 +15,10 @@
 // §3.2 "确定性执行实现": CTA order swizzled over heads/batches for L2 reuse,
 // longest-processing-time-first over batches, and shortest-first over causal
 // kv-tiles for the deterministic dQ reduction):
-//   forward   item = (sequence, head, q-tile m), taken by a static round-robin
-//             over CTAs: q-tiles longest causal row range first (m descending)
-//             with heads varying fastest, which keeps the round-robin balanced.
+//   forward   item = (sequence, head, 256-row unit m: two q-tiles), taken by a
+//             static round-robin over CTAs: units with the longest causal row
+//             range first (m descending), heads varying fastest, which keeps
+//             the round-robin balanced.
 //   backward  item = (sequence, head, kv-tile n); all tiles of one (sequence,
 //             head) are consecutive, so one head's Q, dO and fp32 dQ
 //             accumulator stay in L2 while ~one SM count of its kv-tiles run.
@@ -33,6 +34,7 @@
 namespace attn {
 
 constexpr int kTile = 128;
+constexpr int kFwdRows = 2 * kTile;  // query rows of one forward work item (two Q tiles)
 constexpr int kMaxSeqs = 1024;  // sequences in one variable-length call
 
 // Host-computed tables for variable-length batches (passed by value).
@@ -41,6 +43,7 @@ struct VarlenTables {
   int order[kMaxSeqs];           // sequences, longest first (ties: lower id first)
   int item_start[kMaxSeqs + 1];  // first work item of the k-th sequence in `order`
   int tile_start[kMaxSeqs + 1];  // first q-tile of sequence s in the workspace tile space
+                                 // (item_start counts 256-row units in the forward)
 };
 struct NoTables {};
 
@@ -51,6 +54,7 @@ struct SeqShape {
   int Tq, Tk;      // fixed-length sequence lengths (varlen: unused)
   int nq_tiles;    // fixed-length: ceil(Tq/128)
   int nk_tiles;    // fixed-length: ceil(Tk/128)
+  int nq_units;    // fixed-length: ceil(Tq/256), forward work items per (b, h)
   int n_items;     // number of work items of the kernel
   int causal;
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
@@ -77,11 +81,11 @@ __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const 
                                                       int item, bool forward) {
   Item it;
   int bh, rank;
-  if (forward) {  // tile rank major, (b, h) fastest
+  if (forward) {  // unit rank major, (b, h) fastest; it.tile = 256-row unit
     const int nbh = sh.nseq * sh.H;
     rank = item / nbh;
     bh = item - rank * nbh;
-    it.tile = sh.nq_tiles - 1 - rank;
+    it.tile = sh.nq_units - 1 - rank;
   } else {        // (b, h) major, tile rank fastest
     bh = item / sh.nk_tiles;
     rank = item - bh * sh.nk_tiles;
@@ -112,7 +116,7 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   const int local = item - tb.item_start[lo];
   it.row0 = tb.cu[it.seq];
   it.Lq = it.Lk = tb.cu[it.seq + 1] - it.row0;
-  const int nt = cdiv(it.Lq, kTile);
+  const int nt = cdiv(it.Lq, forward ? kFwdRows : kTile);
   int rank;
   if (forward) {  // tile rank, then head
     rank = local / sh.H;

@@ -9,16 +9,20 @@
 // key/value tiles, with a running row maximum and row sum) and §4.2 (the
 // division by the row sum happens once, after the loop).
 //
-// One CTA (192 threads) per SM, persistent over work items (see
-// attn_common.cuh for the item order):
-//   warps 0-3  softmax: thread r owns query row r of the tile (TMEM lane r)
-//   warp 4     TMA producer: Q tile once per item, K/V tiles into a ring
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM buffers, then
-//              O += P V into a TMEM accumulator
-// Tensor memory: S buffers at columns [0,128) and [128,256), O at [256, 256+dv).
-// P goes through shared memory as bf16 in the 128-byte-swizzled panel layout
-// the MMA reads.  The running maximum is only moved (and O rescaled) when it
-// grows by more than 2^8, so most tiles skip the rescale.
+// One CTA (320 threads) per SM, persistent over work items; an item is two
+// consecutive 128-row Q tiles of one (sequence, head) (see attn_common.cuh for
+// the order):
+//   warps 0-3, 4-7  softmax warpgroup w owns Q tile w: thread r holds query
+//                   row r (TMEM lane r)
+//   warp 8          TMA producer: the two Q tiles once per item, K and V tiles
+//                   into rings of their own
+//   warp 9          MMA issuer: S_w = Q_w K^T and O_w += P_w V
+// Tensor memory: S_0, S_1 at columns [0,128), [128,256), O_0, O_1 after them.
+// P is written back into the S columns as bf16 pairs and read from there by
+// the O += P V product (A operand in tensor memory), so it never touches
+// shared memory.  The two warpgroups alternate: while one computes its P, the
+// tensor core runs the other tile's MMAs.  The running maximum is only moved
+// (and O rescaled) when it grows by more than 2^8, so most tiles skip it.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -28,7 +32,13 @@
 namespace attn {
 namespace {
 
-constexpr int kFwdThreads = 192;
+// Softmax warpgroups 0 and 1; warpgroup 2 holds the TMA warp (8) and the MMA
+// warp (9), warps 10-11 idle.  Launched with 384 x 168 registers; warpgroup 2
+// gives back (168 - 56) x 128, which the two softmax warpgroups take.
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kRegsCtl = 128;
+constexpr uint32_t kRegsSoftmax = 184;
+static_assert(2 * kRegsSoftmax + kRegsCtl <= 3 * 168, "register split");
 constexpr int kPanelBytes = kTile * 128;  // [128 rows][64] bf16
 constexpr int kMaxSmem = 232448;
 
@@ -36,14 +46,15 @@ template <int DQK, int DV>
 struct FwdCfg {
   static constexpr int kQPanels = DQK / 64;
   static constexpr int kVPanels = DV / 64;
-  static constexpr int kQBytes = kQPanels * kPanelBytes;
+  static constexpr int kQTileBytes = kQPanels * kPanelBytes;  // one 128-row Q tile
+  static constexpr int kQBytes = 2 * kQTileBytes;             // the item's two Q tiles
   static constexpr int kKBytes = kQPanels * kPanelBytes;
   static constexpr int kVBytes = kVPanels * kPanelBytes;
-  static constexpr int kPBytes = 2 * kPanelBytes;
-  static constexpr int kFixed = kQBytes + kPBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static constexpr int kBarBytes = 512;
+  // the dynamic shared memory window starts 1024-byte aligned (checked at run time)
+  static constexpr int kFixed = kQBytes + kBarBytes;
   // K and V have rings of their own: S(t) needs only a K slot, so it can be
   // issued while V of the previous tile is still being read by O += P V.
-  // Two K slots at least; V slots from what is left (one suffices).
   static constexpr int kPairsFit = (kMaxSmem - kFixed) / (kKBytes + kVBytes);
   static constexpr int kKStages = kPairsFit >= 4 ? 4 : (kPairsFit >= 2 ? kPairsFit : 2);
   static constexpr int kVStagesFit = (kMaxSmem - kFixed - kKStages * kKBytes) / kVBytes;
@@ -51,27 +62,39 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKBytes;
-  static constexpr int kOffP = kOffV + kVStages * kVBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+  static constexpr int kOffBar = kOffV + kVStages * kVBytes;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes;
+  // Tensor memory: S of Q tile w at [128w, 128w+128) (P, bf16 pairs, over its
+  // first 64 columns), O of Q tile w at [256 + w*DV, 256 + (w+1)*DV).
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmemS = 0;
   static constexpr uint32_t kTmemO = 256;
   static_assert(kVStages >= 1, "shared memory too small");
   static_assert(kKStages <= 4 && kVStages <= 4, "barrier arrays hold 4 stages");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
+  static_assert(kTmemO + 2 * DV <= kTmemCols, "tensor memory budget");
 };
 
-// Barrier slots inside the barrier block.
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done;
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block size");
+
+// kv-tile counts of the two Q tiles of an item (causal: up to the diagonal).
+__device__ __forceinline__ void kv_counts(const SeqShape& sh, const Item& it, int& n0, int& n1) {
+  const int nk = cdiv(it.Lk, kTile);
+  if (sh.causal) {
+    n0 = min(2 * it.tile + 1, nk);
+    n1 = min(2 * it.tile + 2, nk);
+  } else {
+    n0 = n1 = nk;
+  }
+}
 
 template <int DQK, int DV, typename Tables>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -83,14 +106,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const float scale_log2, int* status, const SeqShape sh,
                     const __grid_constant__ Tables tb) {
   using C = FwdCfg<DQK, DV>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the swizzled panels need a 1024-byte aligned window
+    if (threadIdx.x == 0) atomicCAS(status, 0, kStatusInternal);
+    return;
+  }
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kOffBar);
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sK = smem_u32(smem + C::kOffK);
   const uint32_t sV = smem_u32(smem + C::kOffV);
-  const uint32_t sP = smem_u32(smem + C::kOffP);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   Abort ab{&bars->abort_flag, status};
@@ -107,20 +131,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&bars->v_full[s]), 1);
       mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->s_free[b]), 4);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(smem_u32(&bars->s_full[w]), 1);
+      mbar_init(smem_u32(&bars->p_full[w]), 4);
+      mbar_init(smem_u32(&bars->o_done[w]), 1);
     }
-    mbar_init(smem_u32(&bars->p_full), 4);
-    mbar_init(smem_u32(&bars->o_done), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -130,23 +153,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 4) {
+  if (warp >= 8) {
+   regs_dec<kRegsCtl>();
+   if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    {
       uint32_t kv_it = 0, item_iter = 0, q_issued = 0, k_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item(sh, tb, item, true);
-        const int nk = cdiv(it.Lk, kTile);
-        const int nkv = sh.causal ? min(it.tile + 1, nk) : nk;
+        int n0, n1;
+        kv_counts(sh, it, n0, n1);
         if (!(ok = mbar_wait(smem_u32(&bars->q_empty), (item_iter & 1) ^ 1, ab))) break;
-        mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kQBytes);
+        const uint32_t qf = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qf, C::kQBytes);
         q_issued = item_iter + 1;
-        for (int pnl = 0; pnl < C::kQPanels; ++pnl)
-          tma_load_3d(sQ + pnl * kPanelBytes, &tm_q, smem_u32(&bars->q_full), pnl * 64, it.head,
-                      it.row0 + it.tile * kTile);
+        for (int w = 0; w < 2; ++w)
+          for (int pnl = 0; pnl < C::kQPanels; ++pnl)
+            tma_load_3d(sQ + w * C::kQTileBytes + pnl * kPanelBytes, &tm_q, qf, pnl * 64, it.head,
+                        it.row0 + it.tile * kFwdRows + w * kTile);
         const int krow0 = key_row0(sh, it);
-        for (int j = 0; j < nkv; ++j, ++kv_it) {
+        for (int j = 0; j < n1; ++j, ++kv_it) {
           const uint32_t sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           if (!(ok = mbar_wait(smem_u32(&bars->k_empty[sk]), ((kv_it / C::kKStages) & 1) ^ 1, ab)))
             break;
@@ -175,157 +202,177 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (q_issued > 0) mbar_wait_drain(smem_u32(&bars->q_full), (q_issued - 1) & 1);
       }
     }
-  } else if (warp == 5) {
+   } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Order per kv tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) — while one
+    // softmax warpgroup works on its S, the tensor core runs the other's MMAs.
+    {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, DV, false, true);
-      uint32_t kv_it = 0, sc = 0, item_iter = 0;
+      uint32_t kv_it = 0, item_iter = 0, cnt0 = 0, cnt1 = 0;
       bool ok = true;
-      // descriptor bases (each MMA then only adds a constant)
-      const uint64_t bQ_k = kmajor_base(sQ), bP_k = kmajor_base(sP);
-      const uint32_t tO = tmem + C::kTmemO;
-      auto issue_pv = [&](uint32_t t_kv, uint32_t t_s, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full), t_s & 1, ab)) return false;
+      const uint64_t bQ0 = kmajor_base(sQ), bQ1 = kmajor_base(sQ + C::kQTileBytes);
+      auto W = [&](uint64_t& bar, uint32_t parity) -> bool {
+        if (!mbar_wait(smem_u32(&bar), parity, ab)) return false;
         tc_fence_after();
-        const uint32_t sv = t_kv % C::kVStages;
-        if (!mbar_wait(smem_u32(&bars->v_full[sv]), (t_kv / C::kVStages) & 1, ab)) return false;
-        const uint64_t bV = mnmajor_base(sV + sv * C::kVBytes, 128);
-        mma_bf16(tO, bP_k, bV, idO, first ? 0u : 1u);
+        return true;
+      };
+      auto mma_S = [&](uint64_t bQ, uint32_t tS, uint64_t& sfull, uint32_t t) {
+        const uint64_t bK = kmajor_base(sK + (t % C::kKStages) * C::kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_bf16(tS, bQ + kmajor_step(kk, 128), bK + kmajor_step(kk, 128), idS,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&sfull));
+      };
+      auto mma_PV = [&](uint32_t tS, uint32_t tO, uint32_t t, bool first) {  // A = P from TMEM
+        const uint64_t bV = mnmajor_base(sV + (t % C::kVStages) * C::kVBytes, 128);
+        mma_bf16_ts(tO, tS, bV, idO, first ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < kTile / 16; ++kk)
-          mma_bf16(tO, bP_k + kmajor_step(kk, 128), bV + mnmajor_step(kk), idO, 1u);
-        mma_commit(smem_u32(&bars->o_done));
-        mma_commit(smem_u32(&bars->v_empty[sv]));
+          mma_bf16_ts(tO, tS + kk * 8, bV + mnmajor_step(kk), idO, 1u);
+      };
+      const uint32_t tS0 = tmem + C::kTmemS, tS1 = tmem + C::kTmemS + 128;
+      const uint32_t tO0 = tmem + C::kTmemO, tO1 = tmem + C::kTmemO + DV;
+      // one Q tile's step j: wait for its P, O += P V, then S of tile j+1
+      auto step = [&](uint32_t tS, uint32_t tO, uint64_t bQ, uint64_t& pfull, uint64_t& sfull,
+                      uint64_t& odone, uint32_t& cnt, int j, int n, uint32_t t) -> bool {
+        if (j >= n) return true;
+        if (!W(pfull, cnt & 1)) return false;
+        mma_PV(tS, tO, t, j == 0);
+        if (j + 1 == n) mma_commit(smem_u32(&odone));
+        ++cnt;
+        if (j + 1 < n) mma_S(bQ, tS, sfull, t + 1);
         return true;
       };
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item(sh, tb, item, true);
-        const int nk = cdiv(it.Lk, kTile);
-        const int nkv = sh.causal ? min(it.tile + 1, nk) : nk;
-        if (!(ok = mbar_wait(smem_u32(&bars->q_full), item_iter & 1, ab))) break;
-        tc_fence_after();
-        for (int j = 0; j < nkv; ++j) {
+        int n0, n1;
+        kv_counts(sh, it, n0, n1);
+        if (!(ok = W(bars->q_full, item_iter & 1))) break;
+        // S of the first kv tile for both Q tiles
+        if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
+        mma_S(bQ0, tS0, bars->s_full[0], kv_it);
+        mma_S(bQ1, tS1, bars->s_full[1], kv_it);
+        mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
+        if (n1 == 1) mma_commit(smem_u32(&bars->q_empty));
+        for (int j = 0; ok && j < n1; ++j) {
           const uint32_t t = kv_it + j;
-          const uint32_t ts = sc + j;
-          const uint32_t sk = t % C::kKStages;
-          const uint32_t b = ts & 1;
-          if (!(ok = mbar_wait(smem_u32(&bars->k_full[sk]), (t / C::kKStages) & 1, ab))) break;
-          if (!(ok = mbar_wait(smem_u32(&bars->s_free[b]), ((ts >> 1) & 1) ^ 1, ab))) break;
-          tc_fence_after();
-          const uint64_t bK = kmajor_base(sK + sk * C::kKBytes);
-          const uint32_t tS = tmem + C::kTmemS + b * 128;
-#pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            mma_bf16(tS, bQ_k + kmajor_step(kk, 128), bK + kmajor_step(kk, 128), idS,
-                     kk > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&bars->s_full[b]));
-          mma_commit(smem_u32(&bars->k_empty[sk]));
-          if (j == nkv - 1) mma_commit(smem_u32(&bars->q_empty));
-          if (j > 0 && !(ok = issue_pv(t - 1, ts - 1, j == 1))) break;
+          const bool next = j + 1 < n1;
+          if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
+          if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
+            break;
+          if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0, j,
+                          n0, t)))
+            break;
+          if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1, j,
+                          n1, t)))
+            break;
+          mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
+          if (next) {
+            mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
+            if (j + 2 == n1) mma_commit(smem_u32(&bars->q_empty));
+          }
         }
         if (!ok) break;
-        if (!(ok = issue_pv(kv_it + nkv - 1, sc + nkv - 1, nkv == 1))) break;
-        kv_it += nkv;
-        sc += nkv;
+        kv_it += n1;
       }
       if (!ok) {
         mma_commit(smem_u32(&bars->drain));
         mbar_wait_drain(smem_u32(&bars->drain), 0);
       }
     }
+   }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // query row within the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t sc = 0;
+    const int w = warp >> 2;                 // Q tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;    // query row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::kTmemS + w * 128;
+    const uint32_t tO = tmem + lane_base + C::kTmemO + w * DV;
+    uint32_t cnt = 0, items_done = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x) {
       const Item it = decode_item(sh, tb, item, true);
-      const int nk = cdiv(it.Lk, kTile);
-      const int nkv = sh.causal ? min(it.tile + 1, nk) : nk;
-      const int qidx = it.tile * kTile + r;
+      int n0, n1;
+      kv_counts(sh, it, n0, n1);
+      const int nkv = w ? n1 : n0;
+      const int qt = 2 * it.tile + w;           // q-tile index within the sequence
+      const int qidx = qt * kTile + r;
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv; ++j, ++sc) {
-        const uint32_t b = sc & 1;
-        if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full[b]), (sc >> 1) & 1, ab))) break;
+      for (int j = 0; j < nkv; ++j, ++cnt) {
+        if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full[w]), cnt & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::kTmemS + b * 128 + c * 32, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[b]));
         const int kbase = j * kTile;
-        const bool need_mask = (sh.causal && j == nkv - 1) || (kbase + kTile > it.Lk);
-        float rowmax = -INFINITY;
+        const bool need_mask = (sh.causal && j == qt) || (kbase + kTile > it.Lk);
+        // row maximum over 8 independent chains (a single chain is latency-bound)
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(sr[c][e]) * scale_log2;
+            float x = __uint_as_float(sr[c][e]);
             if (need_mask) {
               const int kidx = kbase + c * 32 + e;
               if (kidx >= it.Lk || (sh.causal && kidx > qidx)) x = -INFINITY;
             }
             sr[c][e] = __float_as_uint(x);
-            rowmax = fmaxf(rowmax, x);
+            mx[e & 7] = fmaxf(mx[e & 7], x);
           }
         }
-        const float m_new = fmaxf(m, rowmax);
+        const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // all PV products of this warpgroup issued before this S are complete
+        // (tensor-core work completes in issue order), so O is stable here
+        const float m_new = fmaxf(m, rowmax * scale_log2);
         const bool resc = (m_new - m) > 8.0f;  // also true on the first tile (m = -inf)
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? ex2(m - m_use) : 1.0f;
-        float rs = 0.f;
+        float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // row sum over 4 independent chains
+        uint32_t pk0[32], pk1[32];  // P as bf16 pairs: keys 0-63, 64-127
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float pe = ex2(__uint_as_float(sr[c][e]) - m_use);
-            sr[c][e] = __float_as_uint(pe);
-            rs += pe;
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), scale_log2, -m_use));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), scale_log2, -m_use));
+            rsp[(e >> 1) & 3] += p0 + p1;
+            if (c < 2) pk0[c * 16 + e / 2] = pack_bf16(p0, p1);
+            else pk1[(c - 2) * 16 + e / 2] = pack_bf16(p0, p1);
           }
         }
-        if (j > 0) {
-          // previous P consumed and O up to date
-          if (!(ok = mbar_wait_warp(smem_u32(&bars->o_done), (sc - 1) & 1, ab))) break;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-            for (int c = 0; c < DV / 32; ++c) {
-              uint32_t ov[32];
-              const uint32_t ta = tmem + lane_base + C::kTmemO + c * 32;
-              tmem_ld32(ta, ov);
-              tmem_ld_wait();
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tmem_st32(ta, ov);
-            }
-            tmem_st_wait();
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(tO + c * 32, ov);
           }
         }
-        l = l * alpha + rs;
+        l = l * alpha + ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3]));
         m = m_use;
-        // P row -> shared memory (panel 0: keys 0-63, panel 1: keys 64-127)
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const int c = ch >> 2, e0 = (ch & 3) * 8;
-          const uint32_t addr = sP + (ch >> 3) * kPanelBytes + sw128_offset(r, ch & 7);
-          st_shared_v4(addr,
-                       pack_bf16(__uint_as_float(sr[c][e0 + 0]), __uint_as_float(sr[c][e0 + 1])),
-                       pack_bf16(__uint_as_float(sr[c][e0 + 2]), __uint_as_float(sr[c][e0 + 3])),
-                       pack_bf16(__uint_as_float(sr[c][e0 + 4]), __uint_as_float(sr[c][e0 + 5])),
-                       pack_bf16(__uint_as_float(sr[c][e0 + 6]), __uint_as_float(sr[c][e0 + 7])));
-        }
-        fence_proxy_async_smem();
+        // P (bf16 pairs) over the S columns just read: A operand of O += P V
+        tmem_st32(tS, pk0);
+        tmem_st32(tS + 32, pk1);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[w]));
       }
       if (!ok) break;
       // epilogue: O / l and the log-sum-exp
-      if (!(ok = mbar_wait_warp(smem_u32(&bars->o_done), (sc - 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&bars->o_done[w]), items_done & 1, ab))) break;
+      ++items_done;
       tc_fence_after();
       const bool valid = qidx < it.Lq;
       const float inv_l = 1.0f / l;
@@ -334,7 +381,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + C::kTmemO + c * 32, ov);
+        tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
@@ -359,7 +406,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
