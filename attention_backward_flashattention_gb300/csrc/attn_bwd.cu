@@ -558,25 +558,40 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
         tc_fence_after();
         uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
-        const bool diag = sh.causal && (i == it.tile);
+        // query columns below qmin are masked: all of them for a key past the
+        // sequence end, those before the key on the causal diagonal tile
+        const int qmin = !key_ok ? 64 : ((sh.causal && i == it.tile) ? r - grp * 64 : 0);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sr[32];
           tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64 + c * 32, sr);
           tmem_ld_wait();
+          if (qmin > 0) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int q = c * 32 + e;  // query column within this group
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            float pe[4];
+            for (int e = 0; e < 32; e += 4) {
+              const int q = c * 32 + e;  // query column within this group
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float pe[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              pe[u] = ex2(__uint_as_float(sr[e + u]) * a.scale_log2 - lv[u]);
-              if (!key_ok || (diag && r > grp * 64 + q + u)) pe[u] = 0.f;
+              for (int u = 0; u < 4; ++u)
+                pe[u] = (q + u >= qmin) ? ex2(__uint_as_float(sr[e + u]) * a.scale_log2 - lv[u])
+                                        : 0.f;
+              pk[(q >> 1) + 0] = pack_bf16(pe[0], pe[1]);
+              pk[(q >> 1) + 1] = pack_bf16(pe[2], pe[3]);
             }
-            pk[(q >> 1) + 0] = pack_bf16(pe[0], pe[1]);
-            pk[(q >> 1) + 1] = pack_bf16(pe[2], pe[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const int q = c * 32 + e;
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+              const float p0 = ex2(fmaf(__uint_as_float(sr[e + 0]), a.scale_log2, -l4.x));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -l4.y));
+              const float p2 = ex2(fmaf(__uint_as_float(sr[e + 2]), a.scale_log2, -l4.z));
+              const float p3 = ex2(fmaf(__uint_as_float(sr[e + 3]), a.scale_log2, -l4.w));
+              pk[(q >> 1) + 0] = pack_bf16(p0, p1);
+              pk[(q >> 1) + 1] = pack_bf16(p2, p3);
+            }
           }
         }
         tmem_st32(tmem + lane_base + C::kTmemS + grp * 64, pk);

@@ -314,17 +314,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+        if (need_mask) {  // diagonal or ragged last tile: keys past the limit -> -inf
+          const int klim = min(it.Lk, sh.causal ? qidx + 1 : it.Lk) - kbase;  // keys < klim
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(sr[c][e]);
-            if (need_mask) {
-              const int kidx = kbase + c * 32 + e;
-              if (kidx >= it.Lk || (sh.causal && kidx > qidx)) x = -INFINITY;
+            for (int e = 0; e < 32; ++e) {
+              const float x = (c * 32 + e < klim) ? __uint_as_float(sr[c][e]) : -INFINITY;
+              sr[c][e] = __float_as_uint(x);
+              mx[e & 7] = fmaxf(mx[e & 7], x);
             }
-            sr[c][e] = __float_as_uint(x);
-            mx[e & 7] = fmaxf(mx[e & 7], x);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[c][e]));
           }
         }
         const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
