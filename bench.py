@@ -345,7 +345,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--cpu-rows", type=int, default=384, help="oracle rows per head (cpu_baseline)")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--workload", default=syn.HEADLINE.name,
                     help="fixed-length workload name (profiling runs on smaller cases)")
     ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per head per reference step")
