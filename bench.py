@@ -159,6 +159,20 @@ def oracle_sample(w, rows_per_head, seed=0, x=None):
     return flops / dt / 1e12, dt, oracle.num_threads(), desc
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    job's time); identity on one rank."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(flops_per_rank, world, steps, seconds):
+    """Whole-job throughput: every rank processes `flops_per_rank` per step."""
+    return world * flops_per_rank * steps / seconds / 1e12
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -262,18 +276,15 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / K
 
-    stats = torch.tensor([total_ms, sum(bwd_ms), sum(fwd_ms), sum(main_ms), e2e_ms],
-                         dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
-    total_ms, bwd_sum, fwd_sum, main_sum, e2e_ms = stats.tolist()
+    total_ms, bwd_sum, fwd_sum, main_sum, e2e_ms = max_over_ranks(
+        [total_ms, sum(bwd_ms), sum(fwd_ms), sum(main_ms), e2e_ms], world, dev)
     if rank != 0:
         return None
 
     peaks = _peaks()
     bwd_flops = w.bwd_flops()
     fwd_flops = w.fwd_flops()
-    value = world * bwd_flops * K / (bwd_sum * 1e-3) / 1e12
+    value = job_tflops(bwd_flops, world, K, bwd_sum * 1e-3)
     main_avg_s = main_sum / K * 1e-3
     achieved = bwd_flops / main_avg_s / 1e12
     peak = peaks["bf16_sustained"]
