@@ -257,7 +257,8 @@ struct BwdBars {
   uint64_t kv_full, kv_done, acc_free;
   uint64_t q_full[kMaxStages], q_empty[kMaxStages];    // Q panels + LSE2 + D of a q-tile
   uint64_t do_full[kMaxStages], do_empty[kMaxStages];  // dO panels
-  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
+  uint64_t s_full, p_full, dp_full, dq_full, dq_free;
+  uint64_t ds_half[2];  // dS^T columns 0-31 / 64-95 (half 0) and 32-63 / 96-127 (half 1)
   uint64_t drain;
   int item_slot[2];
   uint32_t tmem_base;
@@ -321,7 +322,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->p_full), 8);
     mbar_init(smem_u32(&bars->dp_full), 1);
-    mbar_init(smem_u32(&bars->ds_full), 8);
+    mbar_init(smem_u32(&bars->ds_half[0]), 8);
+    mbar_init(smem_u32(&bars->ds_half[1]), 8);
     mbar_init(smem_u32(&bars->dq_full), 1);
     mbar_init(smem_u32(&bars->dq_free), 4);
     mbar_init(smem_u32(&bars->drain), 1);
@@ -446,12 +448,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int kk = 1; kk < kTile / 16; ++kk)
           mma_bf16_ts(tdV, tS + p_col(kk), bdO + mnmajor_step(kk), idV, 1u);
       };
-      auto mma_dK = [&](uint32_t st, bool first) {
+      // dK += dS^T Q in two halves: K steps {0,1,4,5} read the dS^T columns the
+      // compute warps finish first, {2,3,6,7} the rest
+      auto mma_dK = [&](uint32_t st, bool first, int half) {
         const uint64_t bQ = mnmajor_base(sQ_of(st), 128);
-        mma_bf16(tdK, bdS_k, bQ, idK, first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 1; kk < kTile / 16; ++kk)
-          mma_bf16(tdK, bdS_k + kmajor_step(kk, 128), bQ + mnmajor_step(kk), idK, 1u);
+        for (int u = 0; u < 4; ++u) {
+          const int kk = (u & 1) + (u >> 1) * 4 + half * 2;
+          mma_bf16(tdK, bdS_k + kmajor_step(kk, 128), bQ + mnmajor_step(kk), idK,
+                   (first && half == 0 && u == 0) ? 0u : 1u);
+        }
       };
       auto mma_dQ = [&]() {
 #pragma unroll
@@ -492,8 +498,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
               if (!(ok = W(bars->q_full[st1], par1))) break;
               mma_S(st1);
             }
-            if (!(ok = W(bars->ds_full, gi & 1))) break;
-            mma_dK(st, first);
+            if (!(ok = W(bars->ds_half[0], gi & 1))) break;
+            mma_dK(st, first, 0);
+            if (!(ok = W(bars->ds_half[1], gi & 1))) break;
+            mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
             if (!C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
             mma_dQ();
@@ -517,8 +525,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mma_dV(st, first);
             mma_dP(st);  // overwrites the S/P columns after dV has read P
             mma_commit(smem_u32(&bars->do_empty[st]));
-            if (!(ok = W(bars->ds_full, gi & 1))) break;
-            mma_dK(st, first);
+            if (!(ok = W(bars->ds_half[0], gi & 1))) break;
+            mma_dK(st, first, 0);
+            if (!(ok = W(bars->ds_half[1], gi & 1))) break;
+            mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
             mma_dQ();
           }
@@ -628,11 +638,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
             st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch), w[0], w[1], w[2], w[3]);
           }
+          // this half of the dS^T columns is ready for dK
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->ds_half[c]));
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
       }
       if (!ok) break;
       __syncwarp();
