@@ -34,7 +34,8 @@ MAX_VARLEN_SEQS = 1024
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
-            "attn_profile_main_kernel", "attn_bwd_noalloc")
+            "attn_profile_main_kernel", "attn_bwd_noalloc", "attn_step_host_scratch_size",
+            "attn_step_host", "attn_step_host_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +81,13 @@ def load():
         lib.attn_profile_main_kernel.restype = I
         lib.attn_debug_set_wait_bias.argtypes = [I]
         lib.attn_debug_set_wait_bias.restype = I
+        lib.attn_step_host_scratch_size.argtypes = [I, I, I, I, I, I, I]
+        lib.attn_step_host_scratch_size.restype = SZ
+        lib.attn_step_host.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, SZ,
+                                       P, P, P, P]
+        lib.attn_step_host.restype = I
+        lib.attn_step_host_status.argtypes = [P, I, I, I, I, I, I, I, P]
+        lib.attn_step_host_status.restype = I
         _lib = lib
         return lib
 
@@ -180,6 +188,29 @@ def attn_debug_set_wait_bias(bias: int) -> int:
     return load().attn_debug_set_wait_bias(int(bias))
 
 
+def attn_step_host_scratch_size(B, H, T, dqk, dv, heads_per_group=0, deterministic=False) -> int:
+    return int(load().attn_step_host_scratch_size(B, H, T, dqk, dv, int(heads_per_group),
+                                                  int(deterministic)))
+
+
+def attn_step_host(q, k, v, dO, o, dq, dk, dv_out, B, H, T, dqk, dv, causal, scale,
+                   deterministic=False, heads_per_group=0, scratch=None, scratch_bytes=0,
+                   stream=None, stream2=None, h2d_stream=None, d2h_stream=None) -> int:
+    """Host tensors in and out (pinned CPU tensors); copies overlapped with the kernels."""
+    opt = lambda s: None if s is None else _stream(s)
+    return load().attn_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(dq),
+                                 _ptr(dk), _ptr(dv_out), B, H, T, dqk, dv, int(causal),
+                                 float(scale), int(deterministic), int(heads_per_group),
+                                 _ptr(scratch), int(scratch_bytes), _stream(stream),
+                                 opt(stream2), opt(h2d_stream), opt(d2h_stream))
+
+
+def attn_step_host_status(scratch, B, H, T, dqk, dv, heads_per_group=0, deterministic=False,
+                          stream=None) -> int:
+    return load().attn_step_host_status(_ptr(scratch), B, H, T, dqk, dv, int(heads_per_group),
+                                        int(deterministic), _stream(stream))
+
+
 def attn_varlen_order(cu_seqlens) -> list:
     cu = _HostInts(cu_seqlens)
     n = len(cu.arr) - 1
@@ -248,3 +279,38 @@ def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dvt
+
+
+def step_host(q, k, v, dO, causal=False, scale=None, deterministic=False, heads_per_group=0,
+              with_o=False, out=None, scratch=None, streams=None, device=None):
+    """Forward + backward of host (B,T,H,d) bf16 tensors through attn_step_host.
+
+    Returns (dq, dk, dv, o) as host tensors (o is None unless with_o).  Pass
+    pinned tensors for overlapped copies; `out` reuses (dq, dk, dv, o) host
+    buffers, `scratch` a device uint8 buffer, `streams` a (compute, compute2,
+    h2d, d2h) tuple (compute2 may be None).  The call is asynchronous: synchronise the compute stream before
+    reading the outputs (this helper does so unless `streams` is given)."""
+    B, T, H, dqk = q.shape
+    dv = v.shape[-1]
+    scale = 1.0 / math.sqrt(dqk) if scale is None else scale
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if out is None:
+        mk = lambda t: torch.empty(t.shape, dtype=torch.bfloat16, pin_memory=True)
+        out = (mk(q), mk(k), mk(v), mk(v) if with_o else None)
+    need = attn_step_host_scratch_size(B, H, T, dqk, dv, heads_per_group, deterministic)
+    if scratch is None or scratch.numel() * scratch.element_size() < need:
+        scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    own = streams is None
+    if own:
+        streams = (torch.cuda.current_stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev),
+                   torch.cuda.Stream(dev))
+    cs, cs2, hs, ds = streams
+    dq, dk, dvt, o = out
+    rc = attn_step_host(q, k, v, dO, o, dq, dk, dvt, B, H, T, dqk, dv, causal, scale,
+                        deterministic, heads_per_group, scratch,
+                        scratch.numel() * scratch.element_size(), cs, cs2, hs, ds)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_step_host")
+    if own:
+        cs.synchronize()
+    return dq, dk, dvt, o

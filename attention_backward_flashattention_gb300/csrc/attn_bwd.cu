@@ -72,6 +72,43 @@ struct RegSplit {
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Optional phase tracing of CTA 0 (compiled in only with -DATTN_TRACE): the
+// recording thread keeps (clock64 << 8 | event) for q-tile steps
+// [kTraceFrom, kTraceFrom + 8) in a local array and copies it to the caller's
+// buffer (64 records per thread, indexed by thread) when the kernel ends.
+#ifdef ATTN_TRACE
+constexpr int kTraceCap = 64;
+#ifndef ATTN_TRACE_FROM
+#define ATTN_TRACE_FROM 40
+#endif
+constexpr uint32_t kTraceFrom = ATTN_TRACE_FROM;
+#define ATTN_TRACE_DECL                 \
+  unsigned long long tr_buf[kTraceCap]; \
+  int tr_n = 0
+#define ATTN_TRACE_EV(ev, step)                                                       \
+  do {                                                                                \
+    if (blockIdx.x == 0 && (step) >= kTraceFrom && (step) < kTraceFrom + 8 &&         \
+        tr_n < kTraceCap)                                                             \
+      tr_buf[tr_n++] = ((unsigned long long)clock64() << 8) | (unsigned)(ev);         \
+  } while (0)
+#define ATTN_TRACE_FLUSH                                                       \
+  do {                                                                         \
+    if (blockIdx.x == 0 && a.trace != nullptr)                                 \
+      for (int t_ = 0; t_ < kTraceCap; ++t_)                                   \
+        a.trace[threadIdx.x * kTraceCap + t_] = t_ < tr_n ? tr_buf[t_] : 0ull; \
+  } while (0)
+#else
+#define ATTN_TRACE_DECL \
+  do {                  \
+  } while (0)
+#define ATTN_TRACE_EV(ev, step) \
+  do {                          \
+  } while (0)
+#define ATTN_TRACE_FLUSH \
+  do {                   \
+  } while (0)
+#endif
+
 // ---------------------------------------------------------------------------
 // Sequence helpers (shared by the memory-bound kernels)
 // ---------------------------------------------------------------------------
@@ -268,6 +305,9 @@ static_assert(sizeof(BwdBars) <= 512, "barrier block size");
 
 struct MainArgs {
   int sem_bias;  // 0; a test sets it so that the ordered dQ wait can never succeed
+#ifdef ATTN_TRACE
+  unsigned long long* trace;  // kMainThreads x kTraceCap records
+#endif
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int64_t dk_row_stride, dv_row_stride;
@@ -301,6 +341,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int lane = threadIdx.x & 31;
   const SeqShape& sh = a.sh;
   Abort ab{&bars->abort_flag, a.ws.header};
+  ATTN_TRACE_DECL;
   auto sQ_of = [&](uint32_t st) { return sStage + st * (C::kQBytes + C::kdOBytes); };
   auto sdO_of = [&](uint32_t st) { return sStage + st * (C::kQBytes + C::kdOBytes) + C::kQBytes; };
 
@@ -380,6 +421,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const int qrow = it.row0 + i * kTile;
           const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
           if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), par, ab))) break;
+          ATTN_TRACE_EV(40, q_it);
           const uint32_t qb = smem_u32(&bars->q_full[st]);
           mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
           for (int p = 0; p < C::kQPanels; ++p)
@@ -388,6 +430,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.dsum + g * kTile, kTile * 4, qb);
           q_issued = q_it + 1;
           if (!(ok = mbar_wait(smem_u32(&bars->do_empty[st]), par, ab))) break;
+          ATTN_TRACE_EV(41, q_it);
           const uint32_t db = smem_u32(&bars->do_full[st]);
           mbar_arrive_expect_tx(db, C::kdOBytes);
           for (int p = 0; p < C::kVPanels; ++p)
@@ -492,22 +535,29 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             const uint32_t par1 = ((q_it + 1) / C::kStages) & 1;
             const bool first = (i == i0), more = (i + 1 < nq);
             if (!(ok = W(bars->p_full, gi & 1))) break;
+            ATTN_TRACE_EV(10, gi);
             mma_dV(st, first);
             mma_commit(smem_u32(&bars->do_empty[st]));
             if (more) {
               if (!(ok = W(bars->q_full[st1], par1))) break;
+              ATTN_TRACE_EV(11, gi);
               mma_S(st1);
             }
             if (!(ok = W(bars->ds_half[0], gi & 1))) break;
+            ATTN_TRACE_EV(12, gi);
             mma_dK(st, first, 0);
             if (!(ok = W(bars->ds_half[1], gi & 1))) break;
+            ATTN_TRACE_EV(15, gi);
             mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
             if (!C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
             mma_dQ();
+            ATTN_TRACE_EV(16, gi);
             if (more) {
               if (C::kDqOnDp && !(ok = W(bars->dq_free, gi & 1))) break;
+              ATTN_TRACE_EV(13, gi);
               if (!(ok = W(bars->do_full[st1], par1))) break;
+              ATTN_TRACE_EV(14, gi);
               mma_dP(st1);
             }
           }
@@ -567,6 +617,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // ---- P^T = exp2(S^T * s*log2e - LSE2), masked; bf16 pairs -> TMEM
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(20, gi);
         uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
         // query columns below qmin are masked: all of them for a key past the
         // sequence end, those before the key on the causal diagonal tile
@@ -609,9 +660,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(21, gi);
         // ---- dS^T = P^T ⊙ (dP^T − D) -> bf16 panel `grp` of sdS
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dp_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(22, gi);
         // the previous dS tile must have been consumed by its dK and dQ products
         if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->dq_full), (gi - 1) & 1, ab))) break;
 #pragma unroll
@@ -643,6 +696,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->ds_half[c]));
+          if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(23 + c, gi);
         }
       }
       if (!ok) break;
@@ -670,6 +724,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int i = i0; i < nq; ++i, ++gi) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && warp == 8) ATTN_TRACE_EV(30, gi);
         uint32_t qv[DQK];
 #pragma unroll
         for (int c = 0; c < DQK / 32; ++c)
@@ -679,6 +734,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+        if (lane == 0 && warp == 8) ATTN_TRACE_EV(31, gi);
         const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
         float* acc = a.ws.dq_acc + g * (kTile * DQK);
         if (a.deterministic) {
@@ -704,6 +760,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           red_add_v4(acc + (c4 * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
                      __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
                      __uint_as_float(qv[c4 * 4 + 3]));
+        if (lane == 0 && warp == 8) ATTN_TRACE_EV(32, gi);
         if (a.deterministic) {
           named_bar_sync(1, 128);
           if (wt == 0) {
@@ -764,6 +821,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
   }
 
+  ATTN_TRACE_FLUSH;
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -810,6 +868,10 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+#ifdef ATTN_TRACE
+unsigned long long* g_trace_buf = nullptr;
+#endif
+
 template <int DQK, int DV, typename Tables>
 cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
   using C = BwdCfg<DQK, DV>;
@@ -837,6 +899,9 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     a.scale_log2 = L.scale_log2;
     a.deterministic = L.deterministic;
     a.sem_bias = L.sem_bias;
+#ifdef ATTN_TRACE
+    a.trace = g_trace_buf;
+#endif
     a.ws = L.ws;
     a.sh = L.sh;
     auto* k = attn_bwd_main_kernel<DQK, DV, Tables>;
@@ -877,6 +942,11 @@ cudaError_t launch_typed(const BwdLaunch& L) {
 }
 
 }  // namespace
+
+#ifdef ATTN_TRACE
+// Trace builds only: buffer of kMainThreads x 64 records for CTA 0 (null = off).
+extern "C" void attn_trace_set(void* buf) { g_trace_buf = static_cast<unsigned long long*>(buf); }
+#endif
 
 int bwd_smem_bytes(int dqk, int dv) {
   if (dqk == 64 && dv == 64) return BwdCfg<64, 64>::kSmemBytes;

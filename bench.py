@@ -247,25 +247,28 @@ def run_ours(args, rank, world):
     if binding.attn_bwd_status(ws) != 0 or binding.attn_fwd_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
-    # e2e: pinned host inputs -> device, forward + backward, gradients -> host
+    # e2e: pinned host inputs -> device, forward + backward, gradients -> host, through the
+    # host-buffer entry point (copies of one head group overlap the kernels of another)
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dO"))
     hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v))
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+    G = args.e2e_heads_per_group
+    scratch_bytes = binding.attn_step_host_scratch_size(B, H, T, dqk, dv, G, w.deterministic)
+    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=dev)
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    stream2 = torch.cuda.Stream(dev) if args.e2e_streams == 2 else None
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        dO.copy_(hdo, non_blocking=True)
-        fwd()
-        bwd()
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dvv, non_blocking=True)
+        rc = binding.attn_step_host(hq, hk, hv, hdo, None, hdq, hdk, hdv, B, H, T, dqk, dv,
+                                    w.causal, w.scale, w.deterministic, G, scratch,
+                                    scratch_bytes, stream, stream2, h2d_stream, d2h_stream)
+        assert rc == 0, rc
 
     e2e_step()
     torch.cuda.synchronize()
+    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+        raise RuntimeError("device status error in the e2e warm-up")
     if world > 1:
         torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -275,6 +278,8 @@ def run_ours(args, rank, world):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / K
+    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+        raise RuntimeError("device status error in the e2e region")
 
     total_ms, bwd_sum, fwd_sum, main_sum, e2e_ms = max_over_ranks(
         [total_ms, sum(bwd_ms), sum(fwd_ms), sum(main_ms), e2e_ms], world, dev)
@@ -313,7 +318,10 @@ def run_ours(args, rank, world):
                      "avg_launch_ms": main_avg_s * 1e3},
         "cpu_baseline": cpu,
         "e2e": {"value": world * bwd_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "api": "attn_step_host (pinned host tensors; forward + backward; copies of "
+                       "one head group overlap the kernels of another)",
+                "heads_per_group": G or -(-H // 2), "compute_streams": args.e2e_streams},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
     }
@@ -361,6 +369,10 @@ def main():
                     help="fixed-length workload name (profiling runs on smaller cases)")
     ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per head per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-heads-per-group", type=int, default=0,
+                    help="head-group size of the e2e pipeline (0: the library's choice)")
+    ap.add_argument("--e2e-streams", type=int, default=1, choices=(1, 2),
+                    help="compute streams of the e2e pipeline")
     args = ap.parse_args()
     WORKLOAD = syn.ALL[args.workload]
     if WORKLOAD.varlen or WORKLOAD.layout != syn.LAYOUT_BTHD:

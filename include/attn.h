@@ -21,7 +21,8 @@
  * softmax runs in fp32; P and dS are rounded to bf16 before they enter the
  * tensor-core products; dQ is accumulated across key tiles in fp32.
  *
- * Memory.  Every pointer is a DEVICE pointer except `cu_seqlens` (host).
+ * Memory.  Every pointer is a DEVICE pointer except `cu_seqlens` (host) and
+ * the tensors of attn_step_host (host).
  * The library allocates no device memory: the caller owns all buffers,
  * including the backward workspace, sized with attn_bwd_workspace_size().
  * Every tensor pointer must be 16-byte aligned.
@@ -163,6 +164,45 @@ int attn_profile_main_kernel(void* event_start, void* event_stop);
  * 优化：2-CTA MMA模式与内存访问优化", has no bound).
  */
 int attn_debug_set_wait_bias(int bias);
+
+/*
+ * Forward + backward for tensors in HOST memory, with the copies overlapped
+ * with the kernels (the step a caller makes when its data starts and ends on
+ * the host).  q, k, v, dO: host (B,T,H,d) bf16 inputs (layout 0, fixed
+ * length, Tq == Tk == T); dq, dk, dv_out: host (B,T,H,d) bf16 outputs; o: host
+ * (B,T,H,dv) bf16 output or NULL (O stays on the device).  Host memory should
+ * be page-locked (cudaHostAlloc / cudaHostRegister): pageable memory works but
+ * its copies do not overlap.  The heads are split into groups of at most
+ * heads_per_group (0 = half the heads, rounded up); the first and the last
+ * group are about half that size, to shorten the pipeline's fill and drain
+ * (H = 16 with the default gives groups of 4, 8, 4).  Each group's slices are copied
+ * in on h2d_stream, computed with attn_fwd + attn_bwd on `stream`, and copied
+ * back on d2h_stream, two groups in flight.  With stream2 != NULL the two
+ * alternating device sets compute on `stream` and stream2, so one group's
+ * kernels can start on SMs that the previous group's last work items leave
+ * idle.  NULL streams mean `stream` (no overlap).  scratch: device memory of at least
+ * attn_step_host_scratch_size() bytes, 256-byte aligned, used only by this
+ * call until `stream` passes its end.  Asynchronous: `stream` waits for every
+ * copy, so synchronising `stream` makes the host outputs valid.  Results are
+ * those of attn_fwd / attn_bwd on the whole tensors (bit-identical with
+ * deterministic = 1).  No counterpart on the pages; it moves the data of the
+ * step that "ops(8)..." §2.1 defines.
+ */
+size_t attn_step_host_scratch_size(int B, int H, int T, int dqk, int dv, int heads_per_group,
+                                   int deterministic);
+int attn_step_host(const void* q, const void* k, const void* v, const void* dO, void* o,
+                   void* dq, void* dk, void* dv_out, int B, int H, int T, int dqk, int dv,
+                   int causal, float scale, int deterministic, int heads_per_group,
+                   void* scratch, size_t scratch_bytes, void* stream, void* stream2,
+                   void* h2d_stream, void* d2h_stream);
+
+/*
+ * Synchronises `stream` and returns the device status of the last
+ * attn_step_host call that used `scratch` with these sizes: ATTN_OK, or the
+ * first group's ATTN_ERR_TIMEOUT (forward or backward).
+ */
+int attn_step_host_status(const void* scratch, int B, int H, int T, int dqk, int dv,
+                          int heads_per_group, int deterministic, void* stream);
 
 /* Static text for an ATTN_* code. */
 const char* attn_strerror(int code);

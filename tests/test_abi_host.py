@@ -110,3 +110,44 @@ def test_varlen_order_longest_first(lib):
     assert binding.attn_varlen_order([0, 10, 20, 25, 35]) == [0, 1, 3, 2]
     with pytest.raises(binding.AttnError):
         binding.attn_varlen_order([0, 10, 5])
+
+
+def _step(**kw):
+    args = dict(q=A, k=A, v=A, dO=A, o=None, dq=A, dk=A, dv_out=A, B=1, H=4, T=256, dqk=64,
+                dv=64, causal=1, scale=0.125, deterministic=0, heads_per_group=0, scratch=A,
+                scratch_bytes=1 << 40, stream=0, stream2=0, h2d_stream=0, d2h_stream=0)
+    args.update(kw)
+    return binding.attn_step_host(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dv_out=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scratch=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scratch=A + 16), binding.ATTN_ERR_INVALID_ARG),    # must be 256-byte aligned
+    (dict(heads_per_group=-1), binding.ATTN_ERR_INVALID_ARG),
+    (dict(T=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dqk=96, dv=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(scratch_bytes=4096), binding.ATTN_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_step_host_rejects(lib, kw, code):
+    assert _step(**kw) == code
+
+
+def test_step_host_scratch_formula(lib):
+    """Two device sets of G heads (q, k, v, dO, o, lse, dq, dk, dv, backward
+    workspace, each rounded to 256 bytes) plus a status word per head."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for (B, H, T, dqk, dv, G, det) in [(1, 16, 32768, 128, 128, 0, 0), (2, 12, 1000, 64, 64, 5, 1),
+                                       (1, 3, 200, 192, 128, 1, 0), (1, 7, 64, 128, 128, 9, 0)]:
+        g = min(G, H) if G else -(-H // 2)
+        rows = B * T
+        eq, ev = rows * g * dqk * 2, rows * g * dv * 2
+        ws = binding.attn_bwd_workspace_size(B, g, T, T, dqk, dv, 0, det)
+        one = 2 * r256(eq) + 2 * r256(ev) + r256(ev) + r256(rows * g * 4) + 2 * r256(eq) \
+            + r256(ev) + r256(ws)
+        assert binding.attn_step_host_scratch_size(B, H, T, dqk, dv, G, det) == \
+            2 * one + r256(H * 4), (B, H, T, dqk, dv, G, det)
+    assert binding.attn_step_host_scratch_size(1, 4, 128, 96, 96) == 0
+    assert binding.attn_step_host_scratch_size(1, 4, 128, 64, 64, -1) == 0
