@@ -295,8 +295,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   uint8_t* base = static_cast<uint8_t*>(workspace);
   L.ws.header = reinterpret_cast<int*>(base);
   L.ws.sem = reinterpret_cast<int*>(base + w.header);
-  L.ws.lse2 = reinterpret_cast<float*>(base + w.header + w.sem);
-  L.ws.dsum = reinterpret_cast<float*>(base + w.header + w.sem + w.stat);
+  L.ws.nlse2 = reinterpret_cast<float*>(base + w.header + w.sem);
+  L.ws.ndsum = reinterpret_cast<float*>(base + w.header + w.sem + w.stat);
   L.ws.dq_acc = reinterpret_cast<float*>(base + w.header + w.sem + 2 * w.stat);
   L.o = o;
   L.dout = dO;

@@ -218,8 +218,10 @@ __global__ void __launch_bounds__(256)
       const int64_t lbase = sh.varlen ? (int64_t)S::row0(sh, tb, s) : (int64_t)s * lse_seq_stride;
       const float l = lse[(int64_t)h * lse_head_stride + lbase + t];
       const int64_t g = ((int64_t)(S::tile_start(sh, tb, s) + t / kTile) * H + h) * kTile + (t % kTile);
-      ws.dsum[g] = part;
-      ws.lse2[g] = l * kLog2e;
+      // stored negated: the main kernel adds them (packed FP32 pairs have no
+      // negated-operand form)
+      ws.ndsum[g] = -part;
+      ws.nlse2[g] = -l * kLog2e;
     }
   }
   // padding rows of each sequence's last q-tile: P must come out as zero there
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(256)
     const int nt = cdiv(L, kTile);
     if (nt == 0 || (nt - 1) * kTile + r < L) continue;
     const int64_t g = ((int64_t)(S::tile_start(sh, tb, s) + nt - 1) * H + h) * kTile + r;
-    ws.dsum[g] = 0.f;
-    ws.lse2[g] = INFINITY;
+    ws.ndsum[g] = 0.f;
+    ws.nlse2[g] = -INFINITY;
   }
   // zero the dQ accumulator
   float4* acc = reinterpret_cast<float4*>(ws.dq_acc);
@@ -251,7 +253,7 @@ struct BwdCfg {
   static constexpr int kVBytes = kVPanels * kPanelBytes;
   static constexpr int kQBytes = kQPanels * kPanelBytes;
   static constexpr int kdOBytes = kVPanels * kPanelBytes;
-  static constexpr int kStatBytes = 2 * kTile * 4;  // lse2 + D of one q-tile
+  static constexpr int kStatBytes = 2 * kTile * 4;  // -LSE2 and -D of one q-tile
   static constexpr int kStageBytes = kQBytes + kdOBytes + kStatBytes;
   static constexpr int kdSBytes = 2 * kPanelBytes;
   static constexpr int kBarBytes = 512;
@@ -426,8 +428,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
           for (int p = 0; p < C::kQPanels; ++p)
             tma_load_3d(sQ_of(st) + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
-          bulk_load(sStat + st * C::kStatBytes, a.ws.lse2 + g * kTile, kTile * 4, qb);
-          bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.dsum + g * kTile, kTile * 4, qb);
+          bulk_load(sStat + st * C::kStatBytes, a.ws.nlse2 + g * kTile, kTile * 4, qb);
+          bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.ndsum + g * kTile, kTile * 4, qb);
           q_issued = q_it + 1;
           if (!(ok = mbar_wait(smem_u32(&bars->do_empty[st]), par, ab))) break;
           ATTN_TRACE_EV(41, q_it);
@@ -612,8 +614,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const bool key_ok = it.tile * kTile + r < it.Lk;
       for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
         const uint32_t st = q_it % C::kStages;
-        const float* lse2 = stat_f + st * (C::kStatBytes / 4) + grp * 64;
-        const float* dsum = lse2 + kTile;
+        const float* nlse2 = stat_f + st * (C::kStatBytes / 4) + grp * 64;  // -LSE * log2(e)
+        const float* ndsum = nlse2 + kTile;                                  // -D
         // ---- P^T = exp2(S^T * s*log2e - LSE2), masked; bf16 pairs -> TMEM
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
         tc_fence_after();
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // query columns below qmin are masked: all of them for a key past the
         // sequence end, those before the key on the causal diagonal tile
         const int qmin = !key_ok ? 64 : ((sh.causal && i == it.tile) ? r - grp * 64 : 0);
+        const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sr[32];
@@ -631,12 +634,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const int q = c * 32 + e;  // query column within this group
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+              const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + q);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
               float pe[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u)
-                pe[u] = (q + u >= qmin) ? ex2(__uint_as_float(sr[e + u]) * a.scale_log2 - lv[u])
+                pe[u] = (q + u >= qmin) ? ex2(fmaf(__uint_as_float(sr[e + u]), a.scale_log2, lv[u]))
                                         : 0.f;
               pk[(q >> 1) + 0] = pack_bf16(pe[0], pe[1]);
               pk[(q >> 1) + 1] = pack_bf16(pe[2], pe[3]);
@@ -645,13 +648,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const int q = c * 32 + e;
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
-              const float p0 = ex2(fmaf(__uint_as_float(sr[e + 0]), a.scale_log2, -l4.x));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -l4.y));
-              const float p2 = ex2(fmaf(__uint_as_float(sr[e + 2]), a.scale_log2, -l4.z));
-              const float p3 = ex2(fmaf(__uint_as_float(sr[e + 3]), a.scale_log2, -l4.w));
-              pk[(q >> 1) + 0] = pack_bf16(p0, p1);
-              pk[(q >> 1) + 1] = pack_bf16(p2, p3);
+              const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + q);
+              // two scores per packed FMA: S * s*log2e - LSE2
+              const uint64_t x01 = fma2(f2(__uint_as_float(sr[e + 0]), __uint_as_float(sr[e + 1])),
+                                        sc2, f2(l4.x, l4.y));
+              const uint64_t x23 = fma2(f2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
+                                        sc2, f2(l4.z, l4.w));
+              pk[(q >> 1) + 0] = pack_bf16(ex2(f2_lo(x01)), ex2(f2_hi(x01)));
+              pk[(q >> 1) + 1] = pack_bf16(ex2(f2_lo(x23)), ex2(f2_hi(x23)));
             }
           }
         }
@@ -675,19 +679,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
           for (int ch = 4 * c; ch < 4 * c + 4; ++ch) {
             const int e0 = (ch & 3) * 8;
-            const float4 da = *reinterpret_cast<const float4*>(dsum + ch * 8);
-            const float4 db = *reinterpret_cast<const float4*>(dsum + ch * 8 + 4);
-            const float dv8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-            // dS = P * (dP - D): the difference in fp32, rounded to bf16, then
-            // multiplied by the bf16 P pair (the product is rounded to bf16 for
-            // the MMAs anyway)
+            const float4 da = *reinterpret_cast<const float4*>(ndsum + ch * 8);
+            const float4 db = *reinterpret_cast<const float4*>(ndsum + ch * 8 + 4);
+            const uint64_t nd2[4] = {f2(da.x, da.y), f2(da.z, da.w), f2(db.x, db.y), f2(db.z, db.w)};
+            // dS = P * (dP - D): the difference in fp32 (packed pairs), rounded
+            // to bf16, then multiplied by the bf16 P pair (the product is
+            // rounded to bf16 for the MMAs anyway)
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const uint32_t pp = pk[ch * 4 + u];
-              const float d0 = __uint_as_float(dr[e0 + 2 * u]) - dv8[2 * u];
-              const float d1 = __uint_as_float(dr[e0 + 2 * u + 1]) - dv8[2 * u + 1];
-              w[u] = mul_bf16x2(pp, pack_bf16(d0, d1));
+              const uint64_t d2 = add2(f2(__uint_as_float(dr[e0 + 2 * u]),
+                                          __uint_as_float(dr[e0 + 2 * u + 1])), nd2[u]);
+              w[u] = mul_bf16x2(pk[ch * 4 + u], pack_bf16(f2_lo(d2), f2_hi(d2)));
             }
             st_shared_v4(sdS + grp * kPanelBytes + sw128_offset(r, ch), w[0], w[1], w[2], w[3]);
           }

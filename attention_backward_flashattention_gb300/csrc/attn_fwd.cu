@@ -40,6 +40,30 @@ constexpr uint32_t kRegsCtl = 128;
 constexpr uint32_t kRegsSoftmax = 184;
 static_assert(2 * kRegsSoftmax + kRegsCtl <= 3 * 168, "register split");
 constexpr int kPanelBytes = kTile * 128;  // [128 rows][64] bf16
+
+// P = 2^(S*scale*log2e - m) for the 128 scores of a row (thread = row): the
+// row sum and the bf16 pairs of keys 0-63 (pk0) and 64-127 (pk1).  The
+// arguments and the sum use packed FP32 pairs (two scores per instruction).
+__device__ __forceinline__ float softmax_exp(const uint32_t (&sr)[4][32], float scale_log2,
+                                             float m_use, uint32_t (&pk0)[32],
+                                             uint32_t (&pk1)[32]) {
+  const uint64_t sc2 = f2(scale_log2, scale_log2), nm2 = f2(-m_use, -m_use);
+  uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four independent chains of pair sums
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const uint64_t x2 = fma2(f2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nm2);
+      const float p0 = ex2(f2_lo(x2)), p1 = ex2(f2_hi(x2));
+      rs2[(e >> 1) & 3] = add2(rs2[(e >> 1) & 3], f2(p0, p1));
+      if (c < 2) pk0[c * 16 + e / 2] = pack_bf16(p0, p1);
+      else pk1[(c - 2) * 16 + e / 2] = pack_bf16(p0, p1);
+    }
+  }
+  const uint64_t s4 = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
+  return f2_lo(s4) + f2_hi(s4);
+}
+
 constexpr int kMaxSmem = 232448;
 
 template <int DQK, int DV>
@@ -329,7 +353,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[c][e]));
+            for (int e = 0; e < 32; e += 2)
+              mx[(e >> 1) & 7] = max3(mx[(e >> 1) & 7], __uint_as_float(sr[c][e]),
+                                      __uint_as_float(sr[c][e + 1]));
           }
         }
         const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -340,19 +366,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool resc = (m_new - m) > 8.0f;  // also true on the first tile (m = -inf)
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? ex2(m - m_use) : 1.0f;
-        float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // row sum over 4 independent chains
         uint32_t pk0[32], pk1[32];  // P as bf16 pairs: keys 0-63, 64-127
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), scale_log2, -m_use));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), scale_log2, -m_use));
-            rsp[(e >> 1) & 3] += p0 + p1;
-            if (c < 2) pk0[c * 16 + e / 2] = pack_bf16(p0, p1);
-            else pk1[(c - 2) * 16 + e / 2] = pack_bf16(p0, p1);
-          }
-        }
+        const float rowsum = softmax_exp(sr, scale_log2, m_use, pk0, pk1);
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st32(tO + c * 32, ov);
           }
         }
-        l = l * alpha + ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3]));
+        l = l * alpha + rowsum;
         m = m_use;
         // P (bf16 pairs) over the S columns just read: A operand of O += P V
         tmem_st32(tS, pk0);

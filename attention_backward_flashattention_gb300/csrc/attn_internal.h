@@ -31,8 +31,8 @@ struct FwdLaunch {
 struct BwdWorkspace {
   int* header;      // [0] status, [1] work-item counter
   int* sem;         // per (q-tile, head): contributions added so far (deterministic mode)
-  float* lse2;      // per (q-tile, head, row): LSE * log2(e); +inf past the sequence end
-  float* dsum;      // per (q-tile, head, row): D = rowsum(dO * O); 0 past the end
+  float* nlse2;     // per (q-tile, head, row): -LSE * log2(e); -inf past the sequence end
+  float* ndsum;     // per (q-tile, head, row): -D = -rowsum(dO * O); 0 past the end
   float* dq_acc;    // per (q-tile, head): [dqk/4][128][4] fp32 partial dQ
 };
 
