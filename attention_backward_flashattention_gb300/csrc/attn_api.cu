@@ -3,6 +3,7 @@
 // launches.  Everything here is host code; all arithmetic runs in the kernels
 // of attn_fwd.cu and attn_bwd.cu.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <atomic>
@@ -184,6 +185,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Tq, int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
              int layout, void* stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;  // running max assumes s > 0
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID_ARG;
@@ -244,6 +246,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv_out || !workspace)
     return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv_out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))

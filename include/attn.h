@@ -80,7 +80,8 @@ extern "C" {
  * Forward: O and (unless lse == NULL, inference mode) LSE.
  * q, k, v: inputs (bf16); o: output (bf16); lse: output (fp32) or NULL.
  * B, H, Tq, Tk, dqk, dv: sizes (see Layouts); causal: 0/1; scale: the s in
- * S = s Q K^T (the pages use 1/sqrt(dqk)); cu_seqlens: NULL or host offsets.
+ * S = s Q K^T, finite and > 0 (the pages use 1/sqrt(dqk)); cu_seqlens: NULL or
+ * host offsets.
  * "ops(8)..." §1.2-1.3 (sdpa returns [O, stats]; stats only when training),
  * §2.1 forward formulas.
  */

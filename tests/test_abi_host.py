@@ -68,6 +68,10 @@ def _bwd(**kw):
     (dict(cu_seqlens=[0, 100, 90], B=2, Tq=90, Tk=90), binding.ATTN_ERR_INVALID_ARG),
     (dict(cu_seqlens=[0, 100, 200], B=2, Tq=300, Tk=300), binding.ATTN_ERR_INVALID_ARG),
     (dict(cu_seqlens=[1, 100, 200], B=2, Tq=200, Tk=200), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.125), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.ATTN_ERR_INVALID_ARG),
 ])
 def test_fwd_rejects(lib, kw, code):
     assert _fwd(**kw) == code
@@ -81,6 +85,7 @@ def test_fwd_rejects(lib, kw, code):
     (dict(workspace_bytes=1024), binding.ATTN_ERR_WORKSPACE_TOO_SMALL),
     (dict(dqk=192, dv=192), binding.ATTN_ERR_UNSUPPORTED),
     (dict(causal=1, Tk=64), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), binding.ATTN_ERR_INVALID_ARG),
 ])
 def test_bwd_rejects(lib, kw, code):
     assert _bwd(**kw) == code

@@ -212,3 +212,18 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     dq2, dk2, dv2 = binding.backward(q, k, v, o, dO, lse, causal=True, scale=w.scale,
                                      deterministic=True, workspace=ws)
     assert binding.attn_bwd_status(ws) == binding.ATTN_OK
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_jumps_between_key_tiles(causal):
+    """Keys of later tiles scaled up so that each row's maximum grows by far
+    more than the forward's lazy-rescale bound (2^8) from one key tile to the
+    next: the rows must be recomputed with the new maximum and O rescaled."""
+    w = W("jump", 1, 2, 1024, 64, 64, causal)
+    x = syn.make_inputs(w, seed=21)
+    k = x["k"].float()
+    for t in range(1, 8):  # key tile t scaled by 1.6^t (score spread grows tile by tile)
+        k[:, t * 128:(t + 1) * 128] *= 1.6 ** t
+    x["k"] = k.bfloat16()
+    g = gc.run_gpu(x, w)
+    gc.assert_within(gc.compare_full(x, w, g), f"jump causal={causal}")
