@@ -24,8 +24,12 @@
  *     (the pages use s = 1/sqrt(d_k)).  dQ = s * dS K and dK = s * dS^T Q.
  *   - The softmax statistic that the forward returns is the natural-log
  *     log-sum-exp of the scaled scores: LSE_i = ln sum_j exp(S_ij).
- *   - Causal visibility is key j visible to query i iff j <= i (top-left
- *     aligned); it is only defined here for Tq == Tk.
+ *   - Causal visibility is key j visible to query i iff j <= i + (Tk - Tq):
+ *     with Tq == Tk that is the §2.2 loop's t2 <= t; with fewer queries than
+ *     keys (separate query and key lengths, "ops(8)..." §1.3's seq_len_q /
+ *     seq_len_kv) the queries are the last Tq positions of the key sequence
+ *     (bottom-right alignment), so every query sees at least one key.  Causal
+ *     with Tq > Tk would leave rows with no visible key and is rejected.
  *
  * Data layout: a "problem" is one (sequence, head) pair.  All matrices are
  * fp64, row-major, one row per token:
@@ -53,21 +57,24 @@
 #define ORACLE_ERR_ARG (-1)
 #define ORACLE_ERR_NOMEM (-2)
 
-static int visible(int causal, int i, int j) {
-  if (ORACLE_PLANT == 3) return causal ? (j < i || (i == 0 && j == 0)) : 1;
-  return causal ? (j <= i) : 1;
+/* Key j visible to query i (causal: j <= i + Tk - Tq). */
+static int visible(int causal, int i, int j, int Tq, int Tk) {
+  const int off = Tk - Tq;
+  if (ORACLE_PLANT == 3) return causal ? (j < i + off || (i == 0 && j == off)) : 1;
+  return causal ? (j <= i + off) : 1;
 }
 
 /* Number of keys query row i may look at (keys 0 .. n-1). */
-static int n_visible(int causal, int i, int Tk) {
+static int n_visible(int causal, int i, int Tq, int Tk) {
   if (!causal) return Tk;
-  if (ORACLE_PLANT == 3 && i > 0) return i;
-  return (i + 1 < Tk) ? i + 1 : Tk;
+  const int off = Tk - Tq;
+  if (ORACLE_PLANT == 3 && i > 0) return i + off;
+  return (i + off + 1 < Tk) ? i + off + 1 : Tk;
 }
 
 static int check_problem(int causal, int Tq, int Tk) {
   if (Tq < 0 || Tk <= 0) return ORACLE_ERR_ARG;
-  if (causal && Tq != Tk) return ORACLE_ERR_ARG;
+  if (causal && Tq > Tk) return ORACLE_ERR_ARG;
   return ORACLE_OK;
 }
 
@@ -159,7 +166,7 @@ int oracle_forward(int nprob, const long long *qrow0, const int *Tq,
         long long qi = qrow0[p] + i;
         const double *Kp = K + krow0[p] * dqk;
         const double *Vp = V + krow0[p] * dv;
-        int n = n_visible(causal, i, Tk[p]);
+        int n = n_visible(causal, i, Tq[p], Tk[p]);
         double lse;
         forward_row(Q + qi * dqk, Kp, Vp, n, dqk, dv, scale, P,
                     O ? O + qi * dv : NULL, &lse);
@@ -219,7 +226,7 @@ static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
   for (int r = 0; r < count; r++) {
     int i = rows ? rows[r] : r;
     if (i < 0 || i >= Tq) continue;
-    int n = n_visible(causal, i, Tk);
+    int n = n_visible(causal, i, Tq, Tk);
     const double *qi = Q + (long long)i * dqk;
     const double *doi = dO + (long long)i * dv;
     double lse;
@@ -346,7 +353,7 @@ int oracle_kv_rows(int Tq, int Tk, int dqk, int dv, int causal, double scale,
     const double *kj = K + (long long)j * dqk;
     const double *vj = V + (long long)j * dv;
     for (int i = 0; i < Tq; i++) {
-      if (!visible(causal, i, j)) continue;
+      if (!visible(causal, i, j, Tq, Tk)) continue;
       const double *qi = Q + (long long)i * dqk;
       const double *doi = dO + (long long)i * dv;
       double s = 0.0;

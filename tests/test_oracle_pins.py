@@ -48,8 +48,10 @@ def _torch_reference(q, k, v, dO, causal, scale):
     vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
     S = scale * qt @ kt.transpose(-1, -2)
     if causal:
+        # query i is position Tk - Tq + i of the key sequence (bottom-right
+        # alignment; top-left when Tq == Tk): keys after it are masked
         Tq, Tk = S.shape[-2:]
-        mask = torch.ones(Tq, Tk, dtype=torch.bool).triu(1)
+        mask = torch.ones(Tq, Tk, dtype=torch.bool).triu(1 + Tk - Tq)
         S = S.masked_fill(mask, float("-inf"))
     P = torch.softmax(S, dim=-1)
     O = P @ vt
@@ -325,7 +327,52 @@ def test_noncausal_rectangular(oracle_mod):
         assert abs(_fd_grad(oracle_mod, q, k, v, dO, False, s, which, idx) - grad[idx]) <= 1e-8
 
 
-def test_rejects_causal_rectangular(oracle_mod):
-    q, k, v, dO = _small(n=1, T=7, d=4, seed=50, Tk=11)
+def test_rejects_causal_with_more_queries_than_keys(oracle_mod):
+    """Bottom-right causal with Tq > Tk would leave query rows that see no key."""
+    q, k, v, dO = _small(n=1, T=11, d=4, seed=50, Tk=7)
     with pytest.raises(ValueError):
         oracle_mod.backward(q, k, v, dO, True, 0.5)
+
+
+def test_causal_rectangular_against_autograd_and_fd(oracle_mod):
+    """Causal with fewer queries than keys (bottom-right): the autograd route
+    with the shifted triangular mask, and central differences of every entry."""
+    q, k, v, dO = _small(n=2, T=6, d=3, seed=51, Tk=10)
+    s = 0.7
+    g = oracle_mod.backward(q, k, v, dO, True, s)
+    t = _torch_reference(q, k, v, dO, True, s)
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(g[key], t[key]) <= 1e-12, key
+    assert float(np.max(np.abs(g["LSE"] - t["LSE"]))) <= 1e-12
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        scale_ref = max(np.max(np.abs(grad)), 1e-30)
+        for idx in np.ndindex(*grad.shape):
+            fd = _fd_grad(oracle_mod, q, k, v, dO, True, s, which, idx)
+            assert abs(fd - grad[idx]) <= 1e-7 * scale_ref, (which, idx)
+
+
+def test_causal_rectangular_is_the_tail_of_a_square_problem(oracle_mod):
+    """The Tq queries of a bottom-right causal problem behave exactly like the
+    last Tq queries of the square causal problem over the same keys (whose
+    other queries have dO = 0, so they add nothing to dK or dV)."""
+    Tq, Tk, d = 5, 12, 4
+    q, k, v, dO = _small(n=1, T=Tq, d=d, seed=52, Tk=Tk)
+    pre_q, _, _, _ = _small(n=1, T=Tk - Tq, d=d, seed=53)
+    qs = np.concatenate([pre_q, q], axis=1)
+    dOs = np.concatenate([np.zeros((1, Tk - Tq, d)), dO], axis=1)
+    s = 0.45
+    rect = oracle_mod.backward(q, k, v, dO, True, s)
+    sq = oracle_mod.backward(qs, k, v, dOs, True, s)
+    for key in ("O", "LSE", "dQ"):
+        np.testing.assert_allclose(rect[key][0], sq[key][0][Tk - Tq:], rtol=1e-13, atol=1e-15)
+    for key in ("dK", "dV"):
+        np.testing.assert_allclose(rect[key], sq[key], rtol=1e-12, atol=1e-15)
+
+
+def test_causal_single_query_sees_every_key(oracle_mod):
+    """Tq = 1 (one decoding step): bottom-right causal equals non-causal."""
+    q, k, v, dO = _small(n=2, T=1, d=5, seed=54, Tk=9)
+    a = oracle_mod.backward(q, k, v, dO, True, 0.4)
+    b = oracle_mod.backward(q, k, v, dO, False, 0.4)
+    for key in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(a[key], b[key])
