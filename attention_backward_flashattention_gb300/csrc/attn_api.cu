@@ -55,7 +55,9 @@ int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const
     for (int b = 0; b < B; ++b)
       if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
   } else {
-    if (causal && Tq != Tk) return ATTN_ERR_UNSUPPORTED;
+    // causal with fewer queries than keys aligns the queries with the last
+    // Tq keys; more queries than keys would leave rows with no visible key
+    if (causal && Tq > Tk) return ATTN_ERR_UNSUPPORTED;
     if ((int64_t)B * Tq > INT32_MAX || (int64_t)B * Tk > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
   }
   // every row of every tensor must fit the 32-bit coordinates of the TMA maps
@@ -212,6 +214,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   L.sh.nk_tiles = cdiv(Tk, kTile);
   L.sh.nq_units = cdiv(Tq, kFwdRows);
   L.sh.causal = causal ? 1 : 0;
+  L.sh.causal_off = varlen ? 0 : Tk - Tq;
   L.sh.descending = 0;
   if (varlen) {
     int n_items = 0, n_qt = 0;
@@ -276,6 +279,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   L.sh.nq_tiles = cdiv(Tq, kTile);
   L.sh.nk_tiles = cdiv(Tk, kTile);
   L.sh.causal = causal ? 1 : 0;
+  L.sh.causal_off = varlen ? 0 : Tk - Tq;
   L.sh.descending = deterministic ? 1 : 0;
   int n_qtiles;
   if (varlen) {

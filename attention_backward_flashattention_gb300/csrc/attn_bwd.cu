@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int p = 0; p < C::kVPanels; ++p)
           tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = sh.causal ? it.tile : 0;
+        const int i0 = first_qtile(sh, it.tile);
         for (int i = i0; i < nq; ++i, ++q_it) {
           const uint32_t st = q_it % C::kStages;
           const uint32_t par = ((q_it / C::kStages) & 1) ^ 1;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (item >= sh.n_items) break;
         const Item it = decode_item(sh, tb, item, false);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = sh.causal ? it.tile : 0;
+        const int i0 = first_qtile(sh, it.tile);
         if (!(ok = W(bars->kv_full, k & 1))) break;
         // dK/dV accumulators of the previous item read out by the epilogue
         if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (item >= sh.n_items) break;
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
-      const int i0 = sh.causal ? it.tile : 0;
+      const int i0 = first_qtile(sh, it.tile);
       const bool key_ok = it.tile * kTile + r < it.Lk;
       for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
         const uint32_t st = q_it % C::kStages;
@@ -623,7 +623,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
         // query columns below qmin are masked: all of them for a key past the
         // sequence end, those before the key on the causal diagonal tile
-        const int qmin = !key_ok ? 64 : ((sh.causal && i == it.tile) ? r - grp * 64 : 0);
+        // (key 128 tile + r is visible to query q iff q >= 128 tile + r - off)
+        const int qmin = !key_ok ? 64
+                                 : (sh.causal ? min(64, max(0, kTile * (it.tile - i) + r -
+                                                                   sh.causal_off - grp * 64))
+                                              : 0);
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -723,7 +727,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
       const int nk = cdiv(it.Lk, kTile);
-      const int i0 = sh.causal ? it.tile : 0;
+      const int i0 = first_qtile(sh, it.tile);
       for (int i = i0; i < nq; ++i, ++gi) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
@@ -743,7 +747,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (a.deterministic) {
           // contributions to q-tile i are added in descending kv-tile order
           int* sem = a.ws.sem + g;
-          const int target = (sh.causal ? (i - it.tile) : (nk - 1 - it.tile)) + a.sem_bias;
+          const int target = last_kvtile(sh, i, nk) - it.tile + a.sem_bias;
           if (wt == 0) {
             const uint64_t t0 = globaltimer();
             while (ld_acquire_gpu(sem) != target) {

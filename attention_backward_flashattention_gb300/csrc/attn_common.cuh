@@ -57,6 +57,9 @@ struct SeqShape {
   int nq_units;    // fixed-length: ceil(Tq/256), forward work items per (b, h)
   int n_items;     // number of work items of the kernel
   int causal;
+  int causal_off;  // causal: key j is visible to query i iff j <= i + causal_off
+                   // (Tk - Tq for fixed length: the queries are the last Tq
+                   // positions of the key sequence; 0 for variable length)
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
 };
 
@@ -129,6 +132,15 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   else it.tile = sh.descending ? nt - 1 - rank : rank;
   it.tile_base = tb.tile_start[it.seq];
   return it;
+}
+
+// Causal: the first q-tile that sees any key of kv-tile `kt` (its rows
+// q >= 128 kt - off), and the last kv-tile that q-tile `qt` sees.
+__device__ __forceinline__ int first_qtile(const SeqShape& sh, int kt) {
+  return sh.causal ? max(0, (kt * kTile - sh.causal_off) / kTile) : 0;
+}
+__device__ __forceinline__ int last_kvtile(const SeqShape& sh, int qt, int nk) {
+  return sh.causal ? min(nk - 1, (qt * kTile + kTile - 1 + sh.causal_off) / kTile) : nk - 1;
 }
 
 // First token row of the keys of a sequence (fixed-length Tk may differ from Tq).

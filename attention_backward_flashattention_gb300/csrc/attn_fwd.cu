@@ -109,15 +109,12 @@ struct FwdBars {
 };
 static_assert(sizeof(FwdBars) <= 512, "barrier block size");
 
-// kv-tile counts of the two Q tiles of an item (causal: up to the diagonal).
+// kv-tile counts of the two Q tiles of an item (causal: up to the last tile
+// that the tile's last query row sees).
 __device__ __forceinline__ void kv_counts(const SeqShape& sh, const Item& it, int& n0, int& n1) {
   const int nk = cdiv(it.Lk, kTile);
-  if (sh.causal) {
-    n0 = min(2 * it.tile + 1, nk);
-    n1 = min(2 * it.tile + 2, nk);
-  } else {
-    n0 = n1 = nk;
-  }
+  n0 = last_kvtile(sh, 2 * it.tile, nk) + 1;
+  n1 = last_kvtile(sh, 2 * it.tile + 1, nk) + 1;
 }
 
 template <int DQK, int DV, typename Tables>
@@ -333,13 +330,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
         tmem_ld_wait();
         const int kbase = j * kTile;
-        const bool need_mask = (sh.causal && j == qt) || (kbase + kTile > it.Lk);
+        // the tile's first query row does not see all of its keys, or it is ragged
+        const bool need_mask = (sh.causal && kbase + kTile - 1 > qt * kTile + sh.causal_off) ||
+                               (kbase + kTile > it.Lk);
         // row maximum over 8 independent chains (a single chain is latency-bound)
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
         if (need_mask) {  // diagonal or ragged last tile: keys past the limit -> -inf
-          const int klim = min(it.Lk, sh.causal ? qidx + 1 : it.Lk) - kbase;  // keys < klim
+          const int klim = min(it.Lk, sh.causal ? qidx + 1 + sh.causal_off : it.Lk) - kbase;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll

@@ -14,8 +14,12 @@
  * forward also returns the softmax statistic the backward needs (§1.3 of the
  * same page: "stats", only in training mode); here that is the natural-log
  * log-sum-exp of the scaled scores, LSE_i = ln sum_j exp(S_ij).
- * Causal masking: key j is visible to query i iff j <= i (the §2.2 CPU loop's
- * t2 <= t), defined for Tq == Tk only.
+ * Causal masking: key j is visible to query i iff j <= i + (Tk - Tq): with
+ * Tq == Tk that is the §2.2 CPU loop's t2 <= t; with fewer queries than keys
+ * (separate query and key lengths, as the cuDNN graph of "ops(8)..." §1.3
+ * allows) the queries are the last Tq positions of the key sequence
+ * (bottom-right alignment).  Causal with Tq > Tk, and causal variable-length
+ * batches with different query and key offsets, are not supported.
  *
  * Precision.  Inputs and outputs are bf16; products accumulate in fp32; the
  * softmax runs in fp32; P and dS are rounded to bf16 before they enter the
@@ -65,7 +69,7 @@ extern "C" {
 
 #define ATTN_OK 0
 #define ATTN_ERR_INVALID_ARG (-1)         /* NULL / misaligned pointer, bad size */
-#define ATTN_ERR_UNSUPPORTED (-2)         /* head sizes, causal with Tq != Tk, ... */
+#define ATTN_ERR_UNSUPPORTED (-2)         /* head sizes, causal with Tq > Tk, ... */
 #define ATTN_ERR_WORKSPACE_TOO_SMALL (-3) /* workspace_bytes below the query */
 #define ATTN_ERR_CUDA (-4)                /* a CUDA runtime call or launch failed */
 #define ATTN_ERR_TIMEOUT (-5)             /* a kernel's bounded wait gave up */

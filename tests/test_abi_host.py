@@ -63,7 +63,7 @@ def _bwd(**kw):
     (dict(layout=7), binding.ATTN_ERR_INVALID_ARG),
     (dict(dqk=96, dv=96), binding.ATTN_ERR_UNSUPPORTED),
     (dict(dqk=128, dv=64), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(Tk=256), binding.ATTN_ERR_UNSUPPORTED),              # causal, Tq != Tk
+    (dict(Tq=256, Tk=128), binding.ATTN_ERR_UNSUPPORTED),      # causal, Tq > Tk
     (dict(layout=1, dqk=192, dv=128), binding.ATTN_ERR_UNSUPPORTED),
     (dict(cu_seqlens=[0, 100, 90], B=2, Tq=90, Tk=90), binding.ATTN_ERR_INVALID_ARG),
     (dict(cu_seqlens=[0, 100, 200], B=2, Tq=300, Tk=300), binding.ATTN_ERR_INVALID_ARG),

@@ -89,6 +89,32 @@ def test_noncausal_rectangular():
     gc.assert_within(gc.compare_full(x, w, g), "rect")
 
 
+@pytest.mark.parametrize("B,H,Tq,Tk,d,dv", [
+    (2, 3, 200, 456, 64, 64),      # offset 256: whole tiles
+    (1, 2, 130, 300, 128, 128),    # offset 170: the diagonal band crosses tiles
+    (2, 2, 1, 300, 128, 128),      # one query (a decoding step): sees every key
+    (1, 2, 129, 131, 192, 128),    # offset 2, ragged on both sides
+    (1, 1, 384, 1000, 64, 64),     # several q-tiles per kv-tile band
+])
+def test_causal_fewer_queries_than_keys(B, H, Tq, Tk, d, dv):
+    """Causal with Tq < Tk: query i sees keys j <= i + Tk - Tq (bottom-right)."""
+    g0 = torch.Generator().manual_seed(60 + Tq)
+    x = {"q": torch.randn(B, Tq, H, d, generator=g0).bfloat16(),
+         "k": torch.randn(B, Tk, H, d, generator=g0).bfloat16(),
+         "v": torch.randn(B, Tk, H, dv, generator=g0).bfloat16(),
+         "dO": torch.randn(B, Tq, H, dv, generator=g0).bfloat16()}
+    w = W("rect_causal", B, H, Tq, d, dv, True)
+    dev = "cuda:0"
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
+    for det in (False, True):
+        dq, dk, dvv = binding.backward(q, k, v, o, dO, lse, causal=True, scale=w.scale,
+                                       deterministic=det)
+        g = {"O": o.float().cpu(), "LSE": lse.cpu(), "dQ": dq.float().cpu(),
+             "dK": dk.float().cpu(), "dV": dvv.float().cpu()}
+        gc.assert_within(gc.compare_full(x, w, g), f"Tq={Tq} Tk={Tk} det={det}")
+
+
 # ---------------------------------------------------------------------------
 # the five workload families at their full sizes
 # ---------------------------------------------------------------------------
