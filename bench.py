@@ -328,6 +328,66 @@ def run_ours(args, rank, world):
     return line
 
 
+def run_fwd_only(args, rank, world):
+    """Inference-mode forward (lse=NULL) of the workload: forward TFLOP/s.
+    A separate measurement (not the bwd headline): `--fwd-only`."""
+    from attention_backward_flashattention_gb300 import binding
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    x = syn.make_inputs(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
+    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        rc = binding.attn_fwd(q, k, v, o, None, B, H, T, T, dqk, dv, w.causal, w.scale, None, 0,
+                              stream)
+        assert rc == 0, rc
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    K = args.steps
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        fwd()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if rank == 0 else None
+    if binding.attn_fwd_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    (total_ms,) = max_over_ranks([a.elapsed_time(b)], world, dev)
+    if rank != 0:
+        return None
+    peaks = _peaks()
+    flops = w.fwd_flops()
+    value = job_tflops(flops, world, K, total_ms * 1e-3)
+    per = flops / (total_ms / K * 1e-3) / 1e12
+    return {
+        "metric": "attn fwd TFLOP/s (bf16, inference: no LSE)", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(w, {"mode": "forward only, lse=NULL"}),
+        "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": per,
+                     "peak": peaks["bf16_sustained"], "unit": UNIT,
+                     "frac": per / peaks["bf16_sustained"],
+                     "frac_of_burst": per / peaks["bf16_burst"], "traffic": None,
+                     "algorithmic_flops_per_launch": flops},
+        "gpu_launches": K, "clocks": clocks,
+    }
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -373,6 +433,8 @@ def main():
                     help="head-group size of the e2e pipeline (0: the library's choice)")
     ap.add_argument("--e2e-streams", type=int, default=1, choices=(1, 2),
                     help="compute streams of the e2e pipeline")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time the inference-mode forward (lse=NULL) instead of the step")
     args = ap.parse_args()
     WORKLOAD = syn.ALL[args.workload]
     if WORKLOAD.varlen or WORKLOAD.layout != syn.LAYOUT_BTHD:
@@ -392,7 +454,7 @@ def main():
             build_mod.build()
         if world > 1:
             torch.distributed.barrier()
-        line = run_ours(args, rank, world)
+        line = run_fwd_only(args, rank, world) if args.fwd_only else run_ours(args, rank, world)
     else:
         line = run_reference(args, rank, world)
     if line is not None:
