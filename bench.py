@@ -111,19 +111,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _traffic_for(kernel_src, kernel_name):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    source is unchanged since the counters were taken; else None."""
+KERNEL_SOURCES = ("attn_bwd.cu", "attn_common.cuh", "attn_internal.h", "ptx.cuh")
+
+
+def kernel_sources_sha256():
+    """SHA-256 over the sources the backward main kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "attention_backward_flashattention_gb300", "csrc", name),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic_for(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since the counters were taken; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel_name)
-    if not rec:
-        return None
-    with open(kernel_src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    if rec.get("source_sha256") != digest:
+    if not rec or rec.get("sources_sha256") != kernel_sources_sha256():
         return None
     return rec.get("bytes_per_launch")
 
@@ -293,8 +302,7 @@ def run_ours(args, rank, world):
     main_avg_s = main_sum / K * 1e-3
     achieved = bwd_flops / main_avg_s / 1e12
     peak = peaks["bf16_sustained"]
-    traffic = _traffic_for(os.path.join(ROOT, "attention_backward_flashattention_gb300", "csrc",
-                                        "attn_bwd.cu"), "attn_bwd_main_kernel")
+    traffic = _traffic_for("attn_bwd_main_kernel")
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         tf, secs, cores, desc = oracle_sample(w, args.cpu_rows, x=x)
