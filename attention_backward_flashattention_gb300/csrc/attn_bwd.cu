@@ -38,9 +38,10 @@
 //                   mode); at the end of an item stores dK and dV
 //   warp 12         TMA producer and work-item claimer
 //   warp 13         MMA issuer, tensor-memory owner (warps 14-15 idle)
-// MMA order per q-tile: ... dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, dV_{i+1} ...
-// so that P_{i+1} is computed while dK_i and dQ_i run (S and dP have their
-// own TMEM columns for d <= 128).
+// MMA order per q-tile: ... dV_i, S_{i+1}, dK_i (first half), dQ_i, dK_i
+// (second half), dP_{i+1}, dV_{i+1} ... so that P_{i+1} is computed while dK_i
+// and dQ_i run (S and dP have their own TMEM columns for d <= 128), and the
+// dQ drain overlaps the second half of dK_i.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -298,6 +299,7 @@ struct BwdBars {
   uint64_t do_full[kMaxStages], do_empty[kMaxStages];  // dO panels
   uint64_t s_full, p_full, dp_full, dq_full, dq_free;
   uint64_t ds_half[2];  // dS^T columns 0-31 / 64-95 (half 0) and 32-63 / 96-127 (half 1)
+  uint64_t ds_free;     // the dK and dQ products are done reading dS^T
   uint64_t drain;
   int item_slot[2];
   uint32_t tmem_base;
@@ -368,6 +370,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(smem_u32(&bars->ds_half[0]), 8);
     mbar_init(smem_u32(&bars->ds_half[1]), 8);
     mbar_init(smem_u32(&bars->dq_full), 1);
+    mbar_init(smem_u32(&bars->ds_free), 1);
     mbar_init(smem_u32(&bars->dq_free), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
@@ -550,11 +553,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mma_dK(st, first, 0);
             if (!(ok = W(bars->ds_half[1], gi & 1))) break;
             ATTN_TRACE_EV(15, gi);
-            mma_dK(st, first, 1);
-            mma_commit(smem_u32(&bars->q_empty[st]));
+            // dQ before the second half of dK: the dQ warpgroup starts draining
+            // (and dP_{i+1} can follow) while dK finishes
             if (!C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
             mma_dQ();
             ATTN_TRACE_EV(16, gi);
+            mma_dK(st, first, 1);
+            mma_commit(smem_u32(&bars->q_empty[st]));
+            mma_commit(smem_u32(&bars->ds_free));
             if (more) {
               if (C::kDqOnDp && !(ok = W(bars->dq_free, gi & 1))) break;
               ATTN_TRACE_EV(13, gi);
@@ -583,6 +589,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
             mma_dQ();
+            mma_commit(smem_u32(&bars->ds_free));
           }
         }
         if (!ok) break;
@@ -674,7 +681,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_after();
         if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(22, gi);
         // the previous dS tile must have been consumed by its dK and dQ products
-        if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->dq_full), (gi - 1) & 1, ab))) break;
+        if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->ds_free), (gi - 1) & 1, ab))) break;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dr[32];
