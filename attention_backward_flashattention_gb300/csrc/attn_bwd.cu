@@ -73,30 +73,26 @@ struct RegSplit {
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Optional phase tracing of CTA 0 (compiled in only with -DATTN_TRACE): the
-// recording thread keeps (clock64 << 8 | event) for q-tile steps
-// [kTraceFrom, kTraceFrom + 8) in a local array and copies it to the caller's
-// buffer (64 records per thread, indexed by thread) when the kernel ends.
+// Optional phase tracing of CTA 0 (compiled in only with -DATTN_TRACE): each
+// recording thread stores (clock64 << 8 | event) for q-tile steps
+// [kTraceFrom, kTraceFrom + 8) straight to the caller's buffer (64 records per
+// thread, indexed by thread; the caller zeroes it).
 #ifdef ATTN_TRACE
 constexpr int kTraceCap = 64;
 #ifndef ATTN_TRACE_FROM
 #define ATTN_TRACE_FROM 40
 #endif
 constexpr uint32_t kTraceFrom = ATTN_TRACE_FROM;
-#define ATTN_TRACE_DECL                 \
-  unsigned long long tr_buf[kTraceCap]; \
-  int tr_n = 0
-#define ATTN_TRACE_EV(ev, step)                                                       \
-  do {                                                                                \
-    if (blockIdx.x == 0 && (step) >= kTraceFrom && (step) < kTraceFrom + 8 &&         \
-        tr_n < kTraceCap)                                                             \
-      tr_buf[tr_n++] = ((unsigned long long)clock64() << 8) | (unsigned)(ev);         \
+#define ATTN_TRACE_DECL int tr_n = 0
+#define ATTN_TRACE_EV(ev, step)                                                              \
+  do {                                                                                       \
+    if (a.trace != nullptr && blockIdx.x == 0 && (step) >= kTraceFrom &&                     \
+        (step) < kTraceFrom + 8 && tr_n < kTraceCap)                                         \
+      a.trace[threadIdx.x * kTraceCap + tr_n++] =                                            \
+          ((unsigned long long)clock64() << 8) | (unsigned)(ev);                             \
   } while (0)
-#define ATTN_TRACE_FLUSH                                                       \
-  do {                                                                         \
-    if (blockIdx.x == 0 && a.trace != nullptr)                                 \
-      for (int t_ = 0; t_ < kTraceCap; ++t_)                                   \
-        a.trace[threadIdx.x * kTraceCap + t_] = t_ < tr_n ? tr_buf[t_] : 0ull; \
+#define ATTN_TRACE_FLUSH \
+  do {                   \
   } while (0)
 #else
 #define ATTN_TRACE_DECL \
@@ -682,6 +678,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(22, gi);
         // the previous dS tile must have been consumed by its dK and dQ products
         if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->ds_free), (gi - 1) & 1, ab))) break;
+        if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(25, gi);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dr[32];
