@@ -55,12 +55,12 @@ def _open(path):
     P = ctypes.c_void_p
     I = ctypes.c_int
     D = ctypes.c_double
-    lib.oracle_forward.argtypes = [I, P, P, P, P, I, I, I, D, P, P, P, P, P, P, P]
+    lib.oracle_forward.argtypes = [I, P, P, P, P, I, I, I, I, I, D, P, P, P, P, P, P, P]
     lib.oracle_forward.restype = I
-    lib.oracle_backward.argtypes = [I, I, P, P, P, P, I, I, I, D, P, P, P, P,
+    lib.oracle_backward.argtypes = [I, I, P, P, P, P, I, I, I, I, I, D, P, P, P, P,
                                     P, P, P, P, P, P, P, P, P, P]
     lib.oracle_backward.restype = I
-    lib.oracle_kv_rows.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, I, P, P]
+    lib.oracle_kv_rows.argtypes = [I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, I, P, P]
     lib.oracle_kv_rows.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
@@ -120,10 +120,19 @@ def _stack_if_uniform(parts):
     return parts
 
 
-def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None):
+def _window(window):
+    """(left, right) bounds of a local window; -1 (or None) leaves a side open."""
+    if window is None:
+        return -1, -1
+    wl, wr = window
+    return (-1 if wl is None else int(wl)), (-1 if wr is None else int(wr))
+
+
+def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None, window=None):
     """O, LSE (natural log) and, when dO is given, D_i = sum_j P_ij dP_ij.
 
     q: [nprob][Tq][dqk] (or list), k: [nprob][Tk][dqk], v: [nprob][Tk][dv].
+    window: (left, right) local-attention bounds (see attn_oracle.c), or None.
     Returns (O, LSE, D) with D None when dO is None.
     """
     lib = lib or _load()
@@ -132,8 +141,9 @@ def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None):
     O = np.zeros((nq, pr.dv))
     LSE = np.zeros(nq)
     Dv = np.zeros(nq) if dO is not None else None
+    wl, wr = _window(window)
     rc = lib.oracle_forward(pr.n, _ptr(pr.qrow0), _ptr(pr.Tq), _ptr(pr.krow0),
-                            _ptr(pr.Tk), pr.dqk, pr.dv, int(causal), float(scale),
+                            _ptr(pr.Tk), pr.dqk, pr.dv, int(causal), wl, wr, float(scale),
                             _ptr(pr.Q), _ptr(pr.K), _ptr(pr.V), _ptr(pr.dO),
                             _ptr(O), _ptr(LSE), _ptr(Dv))
     if rc != 0:
@@ -144,7 +154,7 @@ def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None):
 
 
 def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
-             rows=None, want_matrices: bool = False, lib=None):
+             rows=None, want_matrices: bool = False, lib=None, window=None):
     """Full backward by the chain rule of §2.1.
 
     mode "R": dS_i = P_i * (dP_i - <P_i, dP_i>) (row Jacobian-vector product);
@@ -174,9 +184,10 @@ def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
         tot = int((pr.Tq.astype(np.int64) * pr.Tk).sum())
         Pm = np.zeros(tot)
         dSm = np.zeros(tot)
+    wl, wr = _window(window)
     rc = lib.oracle_backward(0 if mode == "R" else 1, pr.n, _ptr(pr.qrow0),
                              _ptr(pr.Tq), _ptr(pr.krow0), _ptr(pr.Tk), pr.dqk,
-                             pr.dv, int(causal), float(scale), _ptr(pr.Q),
+                             pr.dv, int(causal), wl, wr, float(scale), _ptr(pr.Q),
                              _ptr(pr.K), _ptr(pr.V), _ptr(pr.dO), _ptr(rows_arr),
                              _ptr(nrows), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(O),
                              _ptr(LSE), _ptr(Dv), _ptr(Pm), _ptr(dSm))
@@ -202,7 +213,7 @@ def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
     return out
 
 
-def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None):
+def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None, window=None):
     """dK, dV at the listed key rows of ONE problem, given its LSE and D.
 
     q: [Tq][dqk], k: [Tk][dqk], v: [Tk][dv], dO: [Tq][dv], lse/D: [Tq].
@@ -213,8 +224,9 @@ def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None):
     keys = np.ascontiguousarray(keys, dtype=np.int32)
     dk = np.zeros((len(keys), q.shape[1]))
     dv = np.zeros((len(keys), v.shape[1]))
+    wl, wr = _window(window)
     rc = lib.oracle_kv_rows(q.shape[0], k.shape[0], q.shape[1], v.shape[1],
-                            int(causal), float(scale), _ptr(q), _ptr(k), _ptr(v),
+                            int(causal), wl, wr, float(scale), _ptr(q), _ptr(k), _ptr(v),
                             _ptr(dO), _ptr(lse), _ptr(D), _ptr(keys), len(keys),
                             _ptr(dk), _ptr(dv))
     if rc != 0:
@@ -222,9 +234,9 @@ def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None):
     return dk, dv
 
 
-def loss(q, k, v, dO, causal: bool, scale: float, lib=None) -> float:
+def loss(q, k, v, dO, causal: bool, scale: float, lib=None, window=None) -> float:
     """Scalar L = sum(O * dO) whose gradient the backward returns."""
-    O, _, _ = forward(q, k, v, causal, scale, lib=lib)
+    O, _, _ = forward(q, k, v, causal, scale, lib=lib, window=window)
     if isinstance(O, list):
         return float(sum((o * d).sum() for o, d in zip(O, dO)))
     return float((O * np.asarray(dO)).sum())

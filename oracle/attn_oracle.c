@@ -30,6 +30,13 @@
  *     seq_len_kv) the queries are the last Tq positions of the key sequence
  *     (bottom-right alignment), so every query sees at least one key.  Causal
  *     with Tq > Tk would leave rows with no visible key and is rejected.
+ *   - Local (sliding-window) attention, a mask mode of the kind "深度学习反向
+ *     传播优化：2-CTA MMA模式与内存访问优化" §5.2 keeps as an independent module
+ *     (§5.1: FlexAttention-style variants): with window (wl, wr), wl, wr >= 0,
+ *     key j is visible to query i iff
+ *     i + off - wl <= j <= i + off + wr (off = Tk - Tq; -1 = no bound on that
+ *     side), intersected with the causal bound when causal is set.  The
+ *     visible keys of a row are one contiguous range.
  *
  * Data layout: a "problem" is one (sequence, head) pair.  All matrices are
  * fp64, row-major, one row per token:
@@ -57,24 +64,31 @@
 #define ORACLE_ERR_ARG (-1)
 #define ORACLE_ERR_NOMEM (-2)
 
-/* Key j visible to query i (causal: j <= i + Tk - Tq). */
-static int visible(int causal, int i, int j, int Tq, int Tk) {
+/* Keys visible to query row i: lo .. hi (inclusive), one contiguous range:
+ * causal: j <= i + off; window (wl, wr >= 0): i + off - wl <= j <= i + off + wr;
+ * off = Tk - Tq; -1 leaves that side of the window open. */
+static void visible_range(int causal, int wl, int wr, int i, int Tq, int Tk, int *lo,
+                          int *hi) {
   const int off = Tk - Tq;
-  if (ORACLE_PLANT == 3) return causal ? (j < i + off || (i == 0 && j == off)) : 1;
-  return causal ? (j <= i + off) : 1;
+  int l = 0, h = Tk - 1;
+  if (causal) h = (ORACLE_PLANT == 3 && i > 0) ? i + off - 1 : i + off;
+  if (wr >= 0 && i + off + wr < h) h = i + off + wr;
+  if (wl >= 0 && i + off - wl > l) l = i + off - wl;
+  if (h > Tk - 1) h = Tk - 1;
+  *lo = l;
+  *hi = h;
 }
 
-/* Number of keys query row i may look at (keys 0 .. n-1). */
-static int n_visible(int causal, int i, int Tq, int Tk) {
-  if (!causal) return Tk;
-  const int off = Tk - Tq;
-  if (ORACLE_PLANT == 3 && i > 0) return i + off;
-  return (i + off + 1 < Tk) ? i + off + 1 : Tk;
+static int visible(int causal, int wl, int wr, int i, int j, int Tq, int Tk) {
+  int lo, hi;
+  visible_range(causal, wl, wr, i, Tq, Tk, &lo, &hi);
+  return j >= lo && j <= hi;
 }
 
-static int check_problem(int causal, int Tq, int Tk) {
-  if (Tq < 0 || Tk <= 0) return ORACLE_ERR_ARG;
-  if (causal && Tq > Tk) return ORACLE_ERR_ARG;
+static int check_problem(int causal, int wl, int wr, int Tq, int Tk) {
+  if (Tq < 0 || Tk <= 0 || wl < -1 || wr < -1) return ORACLE_ERR_ARG;
+  /* with more queries than keys a bound could leave a row with no key */
+  if ((causal || wl >= 0 || wr >= 0) && Tq > Tk) return ORACLE_ERR_ARG;
   return ORACLE_OK;
 }
 
@@ -129,14 +143,14 @@ static void dp_row(const double *dout, const double *V, int n, int dv,
  */
 int oracle_forward(int nprob, const long long *qrow0, const int *Tq,
                    const long long *krow0, const int *Tk, int dqk, int dv,
-                   int causal, double scale, const double *Q, const double *K,
-                   const double *V, const double *dO, double *O, double *LSE,
-                   double *D) {
+                   int causal, int wl, int wr, double scale, const double *Q,
+                   const double *K, const double *V, const double *dO, double *O,
+                   double *LSE, double *D) {
   if (nprob < 0 || dqk <= 0 || dv <= 0) return ORACLE_ERR_ARG;
   long long total = 0;
   int maxTk = 1;
   for (int p = 0; p < nprob; p++) {
-    if (check_problem(causal, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
+    if (check_problem(causal, wl, wr, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
     total += Tq[p];
     if (Tk[p] > maxTk) maxTk = Tk[p];
   }
@@ -164,9 +178,11 @@ int oracle_forward(int nprob, const long long *qrow0, const int *Tq,
         int p = lo;
         int i = (int)(r - start[p]);
         long long qi = qrow0[p] + i;
-        const double *Kp = K + krow0[p] * dqk;
-        const double *Vp = V + krow0[p] * dv;
-        int n = n_visible(causal, i, Tq[p], Tk[p]);
+        int jlo, jhi;
+        visible_range(causal, wl, wr, i, Tq[p], Tk[p], &jlo, &jhi);
+        const int n = jhi - jlo + 1;
+        const double *Kp = K + (krow0[p] + jlo) * dqk;
+        const double *Vp = V + (krow0[p] + jlo) * dv;
         double lse;
         forward_row(Q + qi * dqk, Kp, Vp, n, dqk, dv, scale, P,
                     O ? O + qi * dv : NULL, &lse);
@@ -206,7 +222,7 @@ int oracle_forward(int nprob, const long long *qrow0, const int *Tq,
  * cases the full Tq x Tk matrices P and dS of the problem (zero where masked).
  */
 static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
-                            int causal, double scale, const double *Q,
+                            int causal, int wl, int wr, double scale, const double *Q,
                             const double *K, const double *V, const double *dO,
                             const int *rows, int nrows, double *dQ, double *dK,
                             double *dV, double *O, double *LSE, double *D,
@@ -226,14 +242,17 @@ static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
   for (int r = 0; r < count; r++) {
     int i = rows ? rows[r] : r;
     if (i < 0 || i >= Tq) continue;
-    int n = n_visible(causal, i, Tq, Tk);
+    int lo, hi;
+    visible_range(causal, wl, wr, i, Tq, Tk, &lo, &hi);
+    const int n = hi - lo + 1;             /* keys lo .. hi; index j below is key lo + j */
+    const double *Ki = K + (long long)lo * dqk, *Vi = V + (long long)lo * dv;
     const double *qi = Q + (long long)i * dqk;
     const double *doi = dO + (long long)i * dv;
     double lse;
-    forward_row(qi, K, V, n, dqk, dv, scale, P, O ? O + (long long)i * dv : NULL,
+    forward_row(qi, Ki, Vi, n, dqk, dv, scale, P, O ? O + (long long)i * dv : NULL,
                 &lse);
     if (LSE) LSE[i] = lse;
-    dp_row(doi, V, n, dv, dP);
+    dp_row(doi, Vi, n, dv, dP);
     double rowdot = 0.0;
     for (int j = 0; j < n; j++) rowdot += P[j] * dP[j];
     if (D) D[i] = rowdot;
@@ -253,25 +272,25 @@ static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
     if (dV)
       for (int j = 0; j < n; j++)
         for (int c = 0; c < dv; c++)
-          dV[(long long)j * dv + c] +=
-              P[j] * (ORACLE_PLANT == 4 ? dO[(long long)j * dv + c] : doi[c]);
+          dV[(long long)(lo + j) * dv + c] +=
+              P[j] * (ORACLE_PLANT == 4 ? dO[(long long)(lo + j) * dv + c] : doi[c]);
     if (dQ) {
       double *dqi = dQ + (long long)i * dqk;
       for (int c = 0; c < dqk; c++) dqi[c] = 0.0;
       for (int j = 0; j < n; j++)
         for (int c = 0; c < dqk; c++)
           dqi[c] += (ORACLE_PLANT == 1 ? 1.0 : scale) * dS[j] *
-                    K[(long long)j * dqk + c];
+                    Ki[(long long)j * dqk + c];
     }
     if (dK)
       for (int j = 0; j < n; j++)
         for (int c = 0; c < dqk; c++)
-          dK[(long long)j * dqk + c] +=
+          dK[(long long)(lo + j) * dqk + c] +=
               scale * dS[j] * (ORACLE_PLANT == 6 ? K[(long long)i * dqk + c] : qi[c]);
     if (Pfull)
-      for (int j = 0; j < n; j++) Pfull[(long long)i * Tk + j] = P[j];
+      for (int j = 0; j < n; j++) Pfull[(long long)i * Tk + lo + j] = P[j];
     if (dSfull)
-      for (int j = 0; j < n; j++) dSfull[(long long)i * Tk + j] = dS[j];
+      for (int j = 0; j < n; j++) dSfull[(long long)i * Tk + lo + j] = dS[j];
   }
   free(P); free(dP); free(dS);
   return ORACLE_OK;
@@ -285,15 +304,15 @@ static int backward_problem(int mode, int Tq, int Tk, int dqk, int dv,
  */
 int oracle_backward(int mode, int nprob, const long long *qrow0, const int *Tq,
                     const long long *krow0, const int *Tk, int dqk, int dv,
-                    int causal, double scale, const double *Q, const double *K,
-                    const double *V, const double *dO, const int *rows,
+                    int causal, int wl, int wr, double scale, const double *Q,
+                    const double *K, const double *V, const double *dO, const int *rows,
                     const int *nrows, double *dQ, double *dK, double *dV,
                     double *O, double *LSE, double *D, double *Pfull,
                     double *dSfull) {
   if (nprob < 0 || dqk <= 0 || dv <= 0 || (mode != 0 && mode != 1))
     return ORACLE_ERR_ARG;
   for (int p = 0; p < nprob; p++)
-    if (check_problem(causal, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
+    if (check_problem(causal, wl, wr, Tq[p], Tk[p])) return ORACLE_ERR_ARG;
   long long *row_start = (long long *)calloc(nprob + 1, sizeof(long long));
   long long *pt_start = (long long *)calloc(nprob + 1, sizeof(long long));
   if (!row_start || !pt_start) {
@@ -309,7 +328,7 @@ int oracle_backward(int mode, int nprob, const long long *qrow0, const int *Tq,
   for (int p = 0; p < nprob; p++) {
     long long q0 = qrow0[p], k0 = krow0[p];
     int e = backward_problem(
-        mode, Tq[p], Tk[p], dqk, dv, causal, scale, Q + q0 * dqk, K + k0 * dqk,
+        mode, Tq[p], Tk[p], dqk, dv, causal, wl, wr, scale, Q + q0 * dqk, K + k0 * dqk,
         V + k0 * dv, dO + q0 * dv, rows ? rows + row_start[p] : NULL,
         rows ? nrows[p] : 0, dQ ? dQ + q0 * dqk : NULL,
         dK ? dK + k0 * dqk : NULL, dV ? dV + k0 * dv : NULL,
@@ -335,12 +354,12 @@ int oracle_backward(int mode, int nprob, const long long *qrow0, const int *Tq,
  *   dK_j  = s sum_i dS_ij Q_i
  * Parallel over the listed keys.  Outputs are [nkeys][dqk] and [nkeys][dv].
  */
-int oracle_kv_rows(int Tq, int Tk, int dqk, int dv, int causal, double scale,
+int oracle_kv_rows(int Tq, int Tk, int dqk, int dv, int causal, int wl, int wr, double scale,
                    const double *Q, const double *K, const double *V,
                    const double *dO, const double *LSE, const double *D,
                    const int *keys, int nkeys, double *dK_rows,
                    double *dV_rows) {
-  if (check_problem(causal, Tq, Tk) || dqk <= 0 || dv <= 0)
+  if (check_problem(causal, wl, wr, Tq, Tk) || dqk <= 0 || dv <= 0)
     return ORACLE_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int t = 0; t < nkeys; t++) {
@@ -353,7 +372,7 @@ int oracle_kv_rows(int Tq, int Tk, int dqk, int dv, int causal, double scale,
     const double *kj = K + (long long)j * dqk;
     const double *vj = V + (long long)j * dv;
     for (int i = 0; i < Tq; i++) {
-      if (!visible(causal, i, j, Tq, Tk)) continue;
+      if (!visible(causal, wl, wr, i, j, Tq, Tk)) continue;
       const double *qi = Q + (long long)i * dqk;
       const double *doi = dO + (long long)i * dv;
       double s = 0.0;

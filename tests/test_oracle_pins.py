@@ -29,30 +29,42 @@ def _small(n=2, T=16, d=8, dv=None, seed=0, Tk=None):
             _rand((n, Tk, dv), seed + 2), _rand((n, T, dv), seed + 3))
 
 
-def _fd_grad(oracle, q, k, v, dO, causal, scale, which, idx, h=1e-6, lib=None):
+def _fd_grad(oracle, q, k, v, dO, causal, scale, which, idx, h=1e-6, lib=None, window=None):
     """Central difference of L = sum(O * dO) w.r.t. one entry of q, k or v."""
     args = {"q": q, "k": k, "v": v}
     plus = {kk: vv.copy() for kk, vv in args.items()}
     minus = {kk: vv.copy() for kk, vv in args.items()}
     plus[which][idx] += h
     minus[which][idx] -= h
-    Op, _, _ = oracle.forward(plus["q"], plus["k"], plus["v"], causal, scale, lib=lib)
-    Om, _, _ = oracle.forward(minus["q"], minus["k"], minus["v"], causal, scale, lib=lib)
+    Op, _, _ = oracle.forward(plus["q"], plus["k"], plus["v"], causal, scale, lib=lib,
+                              window=window)
+    Om, _, _ = oracle.forward(minus["q"], minus["k"], minus["v"], causal, scale, lib=lib,
+                              window=window)
     return float(((np.asarray(Op) - np.asarray(Om)) * dO).sum() / (2 * h))
 
 
-def _torch_reference(q, k, v, dO, causal, scale):
+def _torch_reference(q, k, v, dO, causal, scale, window=None):
     """PyTorch CPU fp64 autograd of softmax(s Q K^T + mask) V (independent route)."""
     qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
     kt = torch.tensor(k, dtype=torch.float64, requires_grad=True)
     vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
     S = scale * qt @ kt.transpose(-1, -2)
+    Tq, Tk = S.shape[-2:]
+    off = Tk - Tq
+    keep = torch.ones(Tq, Tk, dtype=torch.bool)
     if causal:
         # query i is position Tk - Tq + i of the key sequence (bottom-right
         # alignment; top-left when Tq == Tk): keys after it are masked
-        Tq, Tk = S.shape[-2:]
-        mask = torch.ones(Tq, Tk, dtype=torch.bool).triu(1 + Tk - Tq)
-        S = S.masked_fill(mask, float("-inf"))
+        keep &= torch.ones(Tq, Tk, dtype=torch.bool).tril(off)
+    if window is not None:
+        # local window: keys i+off-left .. i+off+right (a negative bound is open)
+        left, right = window
+        if right >= 0:
+            keep &= torch.ones(Tq, Tk, dtype=torch.bool).tril(off + right)
+        if left >= 0:
+            keep &= torch.ones(Tq, Tk, dtype=torch.bool).triu(off - left)
+    if not bool(keep.all()):
+        S = S.masked_fill(~keep, float("-inf"))
     P = torch.softmax(S, dim=-1)
     O = P @ vt
     lse = torch.logsumexp(S, dim=-1)
@@ -376,3 +388,80 @@ def test_causal_single_query_sees_every_key(oracle_mod):
     b = oracle_mod.backward(q, k, v, dO, False, 0.4)
     for key in ("O", "LSE", "dQ", "dK", "dV"):
         np.testing.assert_array_equal(a[key], b[key])
+
+
+# --------------------------------------------------------------------------
+# local (sliding-window) attention
+# --------------------------------------------------------------------------
+WINDOWS = [((2, 1), False), ((3, 0), False), ((4, -1), False), ((-1, 2), False),
+           ((2, -1), True), ((0, 0), False)]
+
+
+@pytest.mark.parametrize("window,causal", WINDOWS)
+def test_window_against_autograd_and_fd(oracle_mod, window, causal):
+    """Local attention: the autograd route with banded masks, and central
+    differences of every entry (Tq < Tk, so the band is shifted by Tk - Tq)."""
+    q, k, v, dO = _small(n=1, T=7, d=3, seed=70, Tk=10)
+    s = 0.6
+    g = oracle_mod.backward(q, k, v, dO, causal, s, window=window)
+    t = _torch_reference(q, k, v, dO, causal, s, window=window)
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(g[key], t[key]) <= 1e-12, key
+    assert float(np.max(np.abs(g["LSE"] - t["LSE"]))) <= 1e-12
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        ref = max(np.max(np.abs(grad)), 1e-30)
+        for idx in np.ndindex(*grad.shape):
+            fd = _fd_grad(oracle_mod, q, k, v, dO, causal, s, which, idx, window=window)
+            assert abs(fd - grad[idx]) <= 1e-7 * ref, (which, idx)
+
+
+def test_window_special_cases(oracle_mod):
+    q, k, v, dO = _small(n=2, T=9, d=4, seed=71)
+    s = 0.5
+    full = oracle_mod.backward(q, k, v, dO, False, s)
+    causal = oracle_mod.backward(q, k, v, dO, True, s)
+    wide = oracle_mod.backward(q, k, v, dO, False, s, window=(50, 50))
+    open_right = oracle_mod.backward(q, k, v, dO, False, s, window=(-1, 0))
+    for key in ("O", "LSE", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(wide[key], full[key])          # band wider than T
+        np.testing.assert_array_equal(open_right[key], causal[key])  # (open, 0) = causal
+    # (0, 0): each query sees only its own key: O = V, dQ = dK = 0, dV = dO
+    diag = oracle_mod.backward(q, k, v, dO, False, s, window=(0, 0))
+    np.testing.assert_allclose(diag["O"], v, rtol=1e-14)
+    np.testing.assert_allclose(diag["LSE"], s * np.einsum("ntd,ntd->nt", q, k), rtol=1e-13)
+    assert np.max(np.abs(diag["dQ"])) == 0 and np.max(np.abs(diag["dK"])) == 0
+    np.testing.assert_allclose(diag["dV"], dO, rtol=1e-14)
+
+
+def test_window_masks_exactly_the_band(oracle_mod):
+    """P and dS vanish outside the band and rows of P sum to one inside it."""
+    Tq, Tk, (wl, wr) = 6, 11, (2, 3)
+    q, k, v, dO = _small(n=1, T=Tq, d=3, seed=72, Tk=Tk)
+    r = oracle_mod.backward(q, k, v, dO, False, 0.7, mode="E", want_matrices=True,
+                            window=(wl, wr))
+    off = Tk - Tq
+    for i in range(Tq):
+        for j in range(Tk):
+            inside = i + off - wl <= j <= i + off + wr
+            assert (r["P"][0, i, j] > 0) == inside, (i, j)
+            if not inside:
+                assert r["dS"][0, i, j] == 0
+    np.testing.assert_allclose(r["P"][0].sum(-1), 1.0, rtol=1e-14)
+
+
+def test_window_key_rows_match_full(oracle_mod):
+    q, k, v, dO = _small(n=1, T=8, d=4, seed=73, Tk=12)
+    w = (3, 1)
+    g = oracle_mod.backward(q, k, v, dO, True, 0.4, window=w)
+    _, lse, D = oracle_mod.forward(q, k, v, True, 0.4, dO=dO, window=w)
+    keys = np.arange(12)
+    dk, dv = oracle_mod.kv_rows(q[0], k[0], v[0], dO[0], np.asarray(lse)[0], np.asarray(D)[0],
+                                keys, True, 0.4, window=w)
+    np.testing.assert_allclose(dk, g["dK"][0], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dv, g["dV"][0], rtol=1e-12, atol=1e-15)
+
+
+def test_window_rejects_more_queries_than_keys(oracle_mod):
+    q, k, v, dO = _small(n=1, T=9, d=3, seed=74, Tk=5)
+    with pytest.raises(ValueError):
+        oracle_mod.backward(q, k, v, dO, False, 0.5, window=(2, 2))
