@@ -35,7 +35,7 @@ MAX_VARLEN_SEQS = 1024
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
             "attn_profile_main_kernel", "attn_bwd_noalloc", "attn_step_host_scratch_size",
-            "attn_step_host", "attn_step_host_status")
+            "attn_step_host", "attn_step_host_status", "attn_fwd_window", "attn_bwd_window")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,11 @@ def load():
         P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, P]
         lib.attn_fwd.restype = I
+        lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, I, P]
+        lib.attn_fwd_window.restype = I
+        lib.attn_bwd_window.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
+                                        P, I, I, P, SZ, P]
+        lib.attn_bwd_window.restype = I
         lib.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_size.restype = SZ
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P,
@@ -131,6 +136,25 @@ def attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, scale, cu_seqlens=N
     cu = _HostInts(cu_seqlens)
     return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, dqk, dv,
                            int(causal), float(scale), cu.ptr, layout, _stream(stream))
+
+
+def attn_fwd_window(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left, window_right,
+                    scale, cu_seqlens=None, layout=LAYOUT_BTHD, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk,
+                                  dqk, dv, int(causal), int(window_left), int(window_right),
+                                  float(scale), cu.ptr, layout, _stream(stream))
+
+
+def attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
+                    window_left, window_right, scale, cu_seqlens=None, layout=LAYOUT_BTHD,
+                    deterministic=False, workspace=None, workspace_bytes=0, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                  _ptr(dq), _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv,
+                                  int(causal), int(window_left), int(window_right),
+                                  float(scale), cu.ptr, layout, int(deterministic),
+                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen=False, deterministic=False) -> int:
@@ -240,8 +264,9 @@ def _dims(q, k, v, cu_seqlens, layout):
 
 
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BTHD,
-            with_lse=True, stream=None):
-    """O (bf16, like q with v's head size) and LSE (fp32) or None."""
+            with_lse=True, stream=None, window=None):
+    """O (bf16, like q with v's head size) and LSE (fp32) or None.
+    window: (left, right) local-attention bounds (-1: open side), or None."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
     o = torch.empty(q.shape[:-2] + (H, dv), dtype=torch.bfloat16, device=q.device)
@@ -249,15 +274,17 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BT
     if with_lse:
         lse = torch.empty((H, Tq) if cu_seqlens is not None else (B, H, Tq),
                           dtype=torch.float32, device=q.device)
-    rc = attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, scale, cu_seqlens, layout,
-                  stream)
+    wl, wr = (-1, -1) if window is None else window
+    rc = attn_fwd_window(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, wl, wr, scale,
+                         cu_seqlens, layout, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return o, lse
 
 
 def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
-             layout=LAYOUT_BTHD, deterministic=False, workspace=None, stream=None, out=None):
+             layout=LAYOUT_BTHD, deterministic=False, workspace=None, stream=None, out=None,
+             window=None):
     """(dq, dk, dv) as bf16 tensors shaped like q, k, v (a packed buffer for layout 1)."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
@@ -273,9 +300,10 @@ def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
     need = attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, cu_seqlens is not None, deterministic)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    rc = attn_bwd(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, scale,
-                  cu_seqlens, layout, deterministic, workspace,
-                  workspace.numel() * workspace.element_size(), stream)
+    wl, wr = (-1, -1) if window is None else window
+    rc = attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, wl, wr,
+                         scale, cu_seqlens, layout, deterministic, workspace,
+                         workspace.numel() * workspace.element_size(), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dvt

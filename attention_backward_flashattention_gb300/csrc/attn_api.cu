@@ -43,7 +43,8 @@ int num_sms_current() {
 
 // Common shape checks of attn_fwd / attn_bwd.  Returns ATTN_OK or an error.
 int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const int* cu,
-                int layout) {
+                int layout, int wl = -1, int wr = -1) {
+  if (wl < -1 || wr < -1) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || Tq <= 0 || Tk <= 0) return ATTN_ERR_INVALID_ARG;
   if (layout != ATTN_LAYOUT_BTHD && layout != ATTN_LAYOUT_PACKED_QKV) return ATTN_ERR_INVALID_ARG;
   if (!supported_dims(dqk, dv)) return ATTN_ERR_UNSUPPORTED;
@@ -55,9 +56,10 @@ int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const
     for (int b = 0; b < B; ++b)
       if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
   } else {
-    // causal with fewer queries than keys aligns the queries with the last
-    // Tq keys; more queries than keys would leave rows with no visible key
-    if (causal && Tq > Tk) return ATTN_ERR_UNSUPPORTED;
+    // causal (or a local window) with fewer queries than keys aligns the
+    // queries with the last Tq keys; more queries than keys would leave rows
+    // with no visible key
+    if ((causal || wl >= 0 || wr >= 0) && Tq > Tk) return ATTN_ERR_UNSUPPORTED;
     if ((int64_t)B * Tq > INT32_MAX || (int64_t)B * Tk > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
   }
   // every row of every tensor must fit the 32-bit coordinates of the TMA maps
@@ -186,12 +188,21 @@ size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int dqk, int dv, in
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int Tq, int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
              int layout, void* stream) {
+  return attn_fwd_window(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, -1, -1, scale,
+                         cu_seqlens, layout, stream);
+}
+
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int Tq, int Tk, int dqk, int dv, int causal, int window_left,
+                    int window_right, float scale, const int* cu_seqlens, int layout,
+                    void* stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;  // running max assumes s > 0
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID_ARG;
-  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout);
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout, window_left,
+                       window_right);
   if (rc) return rc;
 
   FwdLaunch L;
@@ -214,7 +225,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   L.sh.nk_tiles = cdiv(Tk, kTile);
   L.sh.nq_units = cdiv(Tq, kFwdRows);
   L.sh.causal = causal ? 1 : 0;
-  L.sh.causal_off = varlen ? 0 : Tk - Tq;
+  L.sh.band_off = varlen ? 0 : Tk - Tq;
+  L.sh.wl = window_left;
+  L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = 0;
   if (varlen) {
     int n_items = 0, n_qt = 0;
@@ -247,6 +260,16 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
              int dqk, int dv, int causal, float scale, const int* cu_seqlens, int layout,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal, -1,
+                         -1, scale, cu_seqlens, layout, deterministic, workspace,
+                         workspace_bytes, stream);
+}
+
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq,
+                    int Tk, int dqk, int dv, int causal, int window_left, int window_right,
+                    float scale, const int* cu_seqlens, int layout, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv_out || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -254,7 +277,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv_out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_INVALID_ARG;
-  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout);
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout, window_left,
+                       window_right);
   if (rc) return rc;
   const bool varlen = cu_seqlens != nullptr;
   if (workspace_bytes < attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen, deterministic))
@@ -279,7 +303,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   L.sh.nq_tiles = cdiv(Tq, kTile);
   L.sh.nk_tiles = cdiv(Tk, kTile);
   L.sh.causal = causal ? 1 : 0;
-  L.sh.causal_off = varlen ? 0 : Tk - Tq;
+  L.sh.band_off = varlen ? 0 : Tk - Tq;
+  L.sh.wl = window_left;
+  L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = deterministic ? 1 : 0;
   int n_qtiles;
   if (varlen) {

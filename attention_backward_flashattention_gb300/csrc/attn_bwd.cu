@@ -415,8 +415,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int p = 0; p < C::kVPanels; ++p)
           tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = first_qtile(sh, it.tile);
-        for (int i = i0; i < nq; ++i, ++q_it) {
+        const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+        for (int i = i0; i < i1; ++i, ++q_it) {
           const uint32_t st = q_it % C::kStages;
           const uint32_t par = ((q_it / C::kStages) & 1) ^ 1;
           const int qrow = it.row0 + i * kTile;
@@ -517,11 +517,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (item >= sh.n_items) break;
         const Item it = decode_item(sh, tb, item, false);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = first_qtile(sh, it.tile);
+        const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
         if (!(ok = W(bars->kv_full, k & 1))) break;
         // dK/dV accumulators of the previous item read out by the epilogue
         if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
-        if (!C::kSharedSdP) {
+        if (i1 <= i0) {
+          // no query sees this kv tile (a local window): the epilogue writes
+          // zeros; nothing to compute
+        } else if (!C::kSharedSdP) {
           // S and dP of the first q-tile; afterwards S_{i+1} is issued right
           // after dV_i so that P_{i+1} is computed while dK_i and dQ_i run.
           const uint32_t st0 = q_it % C::kStages;
@@ -530,11 +533,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
           if (!(ok = W(bars->do_full[st0], (q_it / C::kStages) & 1))) break;
           mma_dP(st0);
-          for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+          for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;
             const uint32_t st1 = (q_it + 1) % C::kStages;
             const uint32_t par1 = ((q_it + 1) / C::kStages) & 1;
-            const bool first = (i == i0), more = (i + 1 < nq);
+            const bool first = (i == i0), more = (i + 1 < i1);
             if (!(ok = W(bars->p_full, gi & 1))) break;
             ATTN_TRACE_EV(10, gi);
             mma_dV(st, first);
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
         } else {
           // S and dP share columns, and dQ covers them: one q-tile at a time
-          for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+          for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;
             const uint32_t par = (q_it / C::kStages) & 1;
             const bool first = (i == i0);
@@ -613,9 +616,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (item >= sh.n_items) break;
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
-      const int i0 = first_qtile(sh, it.tile);
-      const bool key_ok = it.tile * kTile + r < it.Lk;
-      for (int i = i0; i < nq; ++i, ++q_it, ++gi) {
+      const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+      const int kidx0 = it.tile * kTile + r;  // this thread's key
+      const bool key_ok = kidx0 < it.Lk;
+      for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
         const uint32_t st = q_it % C::kStages;
         const float* nlse2 = stat_f + st * (C::kStatBytes / 4) + grp * 64;  // -LSE * log2(e)
         const float* ndsum = nlse2 + kTile;                                  // -D
@@ -626,18 +630,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
         // query columns below qmin are masked: all of them for a key past the
         // sequence end, those before the key on the causal diagonal tile
-        // (key 128 tile + r is visible to query q iff q >= 128 tile + r - off)
-        const int qmin = !key_ok ? 64
-                                 : (sh.causal ? min(64, max(0, kTile * (it.tile - i) + r -
-                                                                   sh.causal_off - grp * 64))
-                                              : 0);
+        // key kidx is visible to query q iff kidx - off - wr <= q <= kidx - off + wl:
+        // this group's visible query columns are [qmin, qmax)
+        const int qrel = kidx0 - kTile * i - grp * 64;  // kidx - (first query of the group)
+        const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - sh.band_off - sh.wr)) : 0);
+        const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - sh.band_off + sh.wl + 1)) : 64;
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sr[32];
           tmem_ld32(tmem + lane_base + C::kTmemS + grp * 64 + c * 32, sr);
           tmem_ld_wait();
-          if (qmin > 0) {
+          if (qmin > 0 || qmax < 64) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const int q = c * 32 + e;  // query column within this group
@@ -646,8 +650,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
               float pe[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u)
-                pe[u] = (q + u >= qmin) ? ex2(fmaf(__uint_as_float(sr[e + u]), a.scale_log2, lv[u]))
-                                        : 0.f;
+                pe[u] = (q + u >= qmin && q + u < qmax)
+                            ? ex2(fmaf(__uint_as_float(sr[e + u]), a.scale_log2, lv[u]))
+                            : 0.f;
               pk[(q >> 1) + 0] = pack_bf16(pe[0], pe[1]);
               pk[(q >> 1) + 1] = pack_bf16(pe[2], pe[3]);
             }
@@ -731,8 +736,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
       const int nk = cdiv(it.Lk, kTile);
-      const int i0 = first_qtile(sh, it.tile);
-      for (int i = i0; i < nq; ++i, ++gi) {
+      const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+      for (int i = i0; i < i1; ++i, ++gi) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(30, gi);
@@ -792,6 +797,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + C::kTmemdK + c * 32, v);
         tmem_ld_wait();
+        if (i1 <= i0) {  // no query sees this kv tile: nothing was accumulated
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
         if (key_ok) {
           __nv_bfloat16* dst = a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK + c * 32;
 #pragma unroll
@@ -810,6 +819,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + C::kTmemdV + c * 32, v);
         tmem_ld_wait();
+        if (i1 <= i0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
         if (key_ok) {
           __nv_bfloat16* dst = a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV + c * 32;
 #pragma unroll

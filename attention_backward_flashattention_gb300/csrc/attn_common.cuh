@@ -57,9 +57,12 @@ struct SeqShape {
   int nq_units;    // fixed-length: ceil(Tq/256), forward work items per (b, h)
   int n_items;     // number of work items of the kernel
   int causal;
-  int causal_off;  // causal: key j is visible to query i iff j <= i + causal_off
-                   // (Tk - Tq for fixed length: the queries are the last Tq
-                   // positions of the key sequence; 0 for variable length)
+  // The band of visible keys: key j is visible to query i iff
+  //   i + band_off - wl <= j <= i + band_off + wr   (wl, wr = -1: that side open)
+  // causal is wr = 0; band_off = Tk - Tq for fixed length (the queries are the
+  // last Tq positions of the key sequence), 0 for variable length.
+  int band_off;
+  int wl, wr;
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
 };
 
@@ -134,13 +137,25 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   return it;
 }
 
-// Causal: the first q-tile that sees any key of kv-tile `kt` (its rows
-// q >= 128 kt - off), and the last kv-tile that q-tile `qt` sees.
-__device__ __forceinline__ int first_qtile(const SeqShape& sh, int kt) {
-  return sh.causal ? max(0, (kt * kTile - sh.causal_off) / kTile) : 0;
+// Tile ranges of the band: q-tile qt sees kv-tiles first_kvtile .. last_kvtile,
+// kv-tile kt is seen by q-tiles first_qtile .. last_qtile (a tile pair is in
+// the band when any of its (query, key) pairs is).  Numerators of the clamped
+// bounds may be negative; C++ division truncates toward zero, which the clamp
+// to 0 (first_*) absorbs and last_qtile corrects.
+__device__ __forceinline__ int first_kvtile(const SeqShape& sh, int qt) {
+  return sh.wl >= 0 ? max(0, (qt * kTile + sh.band_off - sh.wl) / kTile) : 0;
 }
 __device__ __forceinline__ int last_kvtile(const SeqShape& sh, int qt, int nk) {
-  return sh.causal ? min(nk - 1, (qt * kTile + kTile - 1 + sh.causal_off) / kTile) : nk - 1;
+  return sh.wr >= 0 ? min(nk - 1, (qt * kTile + kTile - 1 + sh.band_off + sh.wr) / kTile)
+                    : nk - 1;
+}
+__device__ __forceinline__ int first_qtile(const SeqShape& sh, int kt) {
+  return sh.wr >= 0 ? max(0, (kt * kTile - sh.band_off - sh.wr) / kTile) : 0;
+}
+__device__ __forceinline__ int last_qtile(const SeqShape& sh, int kt, int nq) {
+  if (sh.wl < 0) return nq - 1;
+  const int num = kt * kTile + kTile - 1 - sh.band_off + sh.wl;
+  return num < 0 ? -1 : min(nq - 1, num / kTile);
 }
 
 // First token row of the keys of a sequence (fixed-length Tk may differ from Tq).

@@ -25,6 +25,8 @@
 // (and O rescaled) when it grows by more than 2^8, so most tiles skip it.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "attn_common.cuh"
 #include "attn_internal.h"
 #include "ptx.cuh"
@@ -109,12 +111,18 @@ struct FwdBars {
 };
 static_assert(sizeof(FwdBars) <= 512, "barrier block size");
 
-// kv-tile counts of the two Q tiles of an item (causal: up to the last tile
-// that the tile's last query row sees).
-__device__ __forceinline__ void kv_counts(const SeqShape& sh, const Item& it, int& n0, int& n1) {
+// kv-tile ranges [lo_w, hi_w] of the two Q tiles of an item (the band's tiles;
+// lo0 <= lo1 and hi0 <= hi1, and the two ranges leave no gap between them).
+// A Q tile that lies wholly past the sequence end can get an empty band (its
+// rows see no key); it then runs its last tile anyway — its rows are never
+// stored — so that every Q tile takes part in at least one step.
+__device__ __forceinline__ void kv_ranges(const SeqShape& sh, const Item& it, int& lo0, int& hi0,
+                                          int& lo1, int& hi1) {
   const int nk = cdiv(it.Lk, kTile);
-  n0 = last_kvtile(sh, 2 * it.tile, nk) + 1;
-  n1 = last_kvtile(sh, 2 * it.tile + 1, nk) + 1;
+  hi0 = last_kvtile(sh, 2 * it.tile, nk);
+  lo0 = min(first_kvtile(sh, 2 * it.tile), hi0);
+  hi1 = last_kvtile(sh, 2 * it.tile + 1, nk);
+  lo1 = min(first_kvtile(sh, 2 * it.tile + 1), hi1);
 }
 
 template <int DQK, int DV, typename Tables>
@@ -183,8 +191,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item(sh, tb, item, true);
-        int n0, n1;
-        kv_counts(sh, it, n0, n1);
+        int lo0, hi0, lo1, hi1;
+        kv_ranges(sh, it, lo0, hi0, lo1, hi1);
         if (!(ok = mbar_wait(smem_u32(&bars->q_empty), (item_iter & 1) ^ 1, ab))) break;
         const uint32_t qf = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qf, C::kQBytes);
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_load_3d(sQ + w * C::kQTileBytes + pnl * kPanelBytes, &tm_q, qf, pnl * 64, it.head,
                         it.row0 + it.tile * kFwdRows + w * kTile);
         const int krow0 = key_row0(sh, it);
-        for (int j = 0; j < n1; ++j, ++kv_it) {
+        for (int j = lo0; j <= hi1; ++j, ++kv_it) {  // every kv tile either Q tile sees
           const uint32_t sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           if (!(ok = mbar_wait(smem_u32(&bars->k_empty[sk]), ((kv_it / C::kKStages) & 1) ^ 1, ab)))
             break;
@@ -255,48 +263,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       const uint32_t tS0 = tmem + C::kTmemS, tS1 = tmem + C::kTmemS + 128;
       const uint32_t tO0 = tmem + C::kTmemO, tO1 = tmem + C::kTmemO + DV;
-      // one Q tile's step j: wait for its P, O += P V, then S of tile j+1
+      // one Q tile's step at kv tile j (ring index t): if j is in its range
+      // [lo, hi], wait for its P and do O += P V; then S of kv tile j+1 if that
+      // is in its range
       auto step = [&](uint32_t tS, uint32_t tO, uint64_t bQ, uint64_t& pfull, uint64_t& sfull,
-                      uint64_t& odone, uint32_t& cnt, int j, int n, uint32_t t) -> bool {
-        if (j >= n) return true;
-        if (!W(pfull, cnt & 1)) return false;
-        mma_PV(tS, tO, t, j == 0);
-        if (j + 1 == n) mma_commit(smem_u32(&odone));
-        ++cnt;
-        if (j + 1 < n) mma_S(bQ, tS, sfull, t + 1);
+                      uint64_t& odone, uint32_t& cnt, int j, int lo, int hi, uint32_t t) -> bool {
+        if (j >= lo && j <= hi) {
+          if (!W(pfull, cnt & 1)) return false;
+          mma_PV(tS, tO, t, j == lo);
+          if (j == hi) mma_commit(smem_u32(&odone));
+          ++cnt;
+        }
+        if (j + 1 >= lo && j + 1 <= hi) mma_S(bQ, tS, sfull, t + 1);
         return true;
       };
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item(sh, tb, item, true);
-        int n0, n1;
-        kv_counts(sh, it, n0, n1);
+        int lo0, hi0, lo1, hi1;
+        kv_ranges(sh, it, lo0, hi0, lo1, hi1);
+        const int n = hi1 - lo0 + 1;  // kv tiles loaded for the item, from lo0
         if (!(ok = W(bars->q_full, item_iter & 1))) break;
-        // S of the first kv tile for both Q tiles
+        // S of the first kv tile (tile 1 joins later when its band starts later)
         if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
         mma_S(bQ0, tS0, bars->s_full[0], kv_it);
-        mma_S(bQ1, tS1, bars->s_full[1], kv_it);
+        if (lo1 == lo0) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
         mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
-        if (n1 == 1) mma_commit(smem_u32(&bars->q_empty));
-        for (int j = 0; ok && j < n1; ++j) {
-          const uint32_t t = kv_it + j;
-          const bool next = j + 1 < n1;
+        if (n == 1) mma_commit(smem_u32(&bars->q_empty));
+        for (int r = 0; ok && r < n; ++r) {
+          const int j = lo0 + r;
+          const uint32_t t = kv_it + r;
+          const bool next = r + 1 < n;
           if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
           if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
             break;
           if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0, j,
-                          n0, t)))
+                          lo0, hi0, t)))
             break;
           if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1, j,
-                          n1, t)))
+                          lo1, hi1, t)))
             break;
           mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
           if (next) {
             mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
-            if (j + 2 == n1) mma_commit(smem_u32(&bars->q_empty));
+            if (r + 2 == n) mma_commit(smem_u32(&bars->q_empty));  // after the last S
           }
         }
         if (!ok) break;
-        kv_it += n1;
+        kv_it += n;
       }
       if (!ok) {
         mma_commit(smem_u32(&bars->drain));
@@ -316,13 +329,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x) {
       const Item it = decode_item(sh, tb, item, true);
-      int n0, n1;
-      kv_counts(sh, it, n0, n1);
-      const int nkv = w ? n1 : n0;
+      int lo0, hi0, lo1, hi1;
+      kv_ranges(sh, it, lo0, hi0, lo1, hi1);
+      const int jlo = w ? lo1 : lo0, jhi = w ? hi1 : hi0;
       const int qt = 2 * it.tile + w;           // q-tile index within the sequence
       const int qidx = qt * kTile + r;
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv; ++j, ++cnt) {
+      for (int j = jlo; j <= jhi; ++j, ++cnt) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full[w]), cnt & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[4][32];
@@ -330,20 +343,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
         tmem_ld_wait();
         const int kbase = j * kTile;
-        // the tile's first query row does not see all of its keys, or it is ragged
-        const bool need_mask = (sh.causal && kbase + kTile - 1 > qt * kTile + sh.causal_off) ||
-                               (kbase + kTile > it.Lk);
+        // some row of the tile does not see all of its keys: the band's right
+        // edge (first row) or left edge (last row) crosses it, or it is ragged
+        const bool need_mask =
+            (sh.wr >= 0 && kbase + kTile - 1 > qt * kTile + sh.band_off + sh.wr) ||
+            (sh.wl >= 0 && kbase < qt * kTile + kTile - 1 + sh.band_off - sh.wl) ||
+            (kbase + kTile > it.Lk);
         // row maximum over 8 independent chains (a single chain is latency-bound)
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-        if (need_mask) {  // diagonal or ragged last tile: keys past the limit -> -inf
-          const int klim = min(it.Lk, sh.causal ? qidx + 1 + sh.causal_off : it.Lk) - kbase;
+        if (need_mask) {  // edge or ragged tile: keys outside the row's band -> -inf
+          // this row's visible keys, relative to the tile: [klo, khi)
+          const int klo = sh.wl >= 0 ? qidx + sh.band_off - sh.wl - kbase : INT_MIN / 2;
+          const int khi =
+              min(it.Lk, sh.wr >= 0 ? qidx + sh.band_off + sh.wr + 1 : it.Lk) - kbase;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float x = (c * 32 + e < klim) ? __uint_as_float(sr[c][e]) : -INFINITY;
+              const float x = (c * 32 + e >= klo && c * 32 + e < khi) ? __uint_as_float(sr[c][e])
+                                                                      : -INFINITY;
               sr[c][e] = __float_as_uint(x);
               mx[e & 7] = fmaxf(mx[e & 7], x);
             }
@@ -362,12 +382,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // all PV products of this warpgroup issued before this S are complete
         // (tensor-core work completes in issue order), so O is stable here
         const float m_new = fmaxf(m, rowmax * scale_log2);
-        const bool resc = (m_new - m) > 8.0f;  // also true on the first tile (m = -inf)
-        const float m_use = resc ? m_new : m;
+        // a row that has seen no key yet (its band starts in a later tile of
+        // the Q tile's range) keeps m = -inf; its P row is exp2(-inf) = 0
+        const bool none = need_mask && m_new == -INFINITY;  // unmasked tiles show every key
+        const bool resc = !none && (m_new - m) > 8.0f;  // also true on a row's first keys
+        const float m_use = none ? 0.f : (resc ? m_new : m);
         const float alpha = resc ? ex2(m - m_use) : 1.0f;
         uint32_t pk0[32], pk1[32];  // P as bf16 pairs: keys 0-63, 64-127
         const float rowsum = softmax_exp(sr, scale_log2, m_use, pk0, pk1);
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > jlo && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t ov[32];
@@ -379,7 +402,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         l = l * alpha + rowsum;
-        m = m_use;
+        m = none ? -INFINITY : m_use;
         // P (bf16 pairs) over the S columns just read: A operand of O += P V
         tmem_st32(tS, pk0);
         tmem_st32(tS + 32, pk1);

@@ -94,6 +94,23 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int layout, void* stream);
 
 /*
+ * Local (sliding-window) attention: as attn_fwd, with key j visible to query i
+ * iff  i + (Tk - Tq) - window_left <= j <= i + (Tk - Tq) + window_right
+ * (each bound >= 0, or -1 for no bound on that side; variable-length batches
+ * use Tk - Tq = 0 within each sequence), intersected with the causal bound
+ * when causal = 1.  (-1, -1) is attn_fwd; (-1, 0) is causal.  A window needs
+ * Tq <= Tk.  A mask mode in the sense of "深度学习反向传播优化：2-CTA MMA模式与
+ * 内存访问优化" §5.1-5.2 (FlexAttention-style variants as independent mask
+ * modules): the kernels visit only the tiles the band touches and mask the
+ * band's edge tiles per element.  Returns ATTN_ERR_INVALID_ARG for bounds
+ * below -1.
+ */
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int Tq, int Tk, int dqk, int dv, int causal, int window_left,
+                    int window_right, float scale, const int* cu_seqlens, int layout,
+                    void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for these sizes (varlen: 1 when
  * cu_seqlens will be given; Tq is then the total token count).  The
  * workspace holds the fp32 dQ accumulator, D and LSE*log2(e) per query row,
@@ -117,6 +134,16 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
              int dqk, int dv, int causal, float scale, const int* cu_seqlens, int layout,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of attn_fwd_window (same window arguments; lse from that forward).
+ * Keys that no query sees get dK = dV = 0.
+ */
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq,
+                    int Tk, int dqk, int dv, int causal, int window_left, int window_right,
+                    float scale, const int* cu_seqlens, int layout, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward for callers that cannot allocate device memory (a plugin whose host

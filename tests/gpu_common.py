@@ -16,7 +16,7 @@ TOL_GRAD = 1e-2
 TOL_LSE = 1e-4
 
 
-def run_gpu(x, w, deterministic=None, with_lse=True):
+def run_gpu(x, w, deterministic=None, with_lse=True, window=None):
     """Forward + backward of workload ``w`` on inputs ``x`` (CPU bf16 tensors)."""
     dev = torch.device("cuda:0")
     det = w.deterministic if deterministic is None else deterministic
@@ -29,9 +29,10 @@ def run_gpu(x, w, deterministic=None, with_lse=True):
         q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     dO = x["dO"].to(dev)
     o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, cu_seqlens=cu_list,
-                             layout=w.layout, with_lse=True)
+                             layout=w.layout, with_lse=True, window=window)
     dq, dk, dv = binding.backward(q, k, v, o, dO, lse, causal=w.causal, scale=w.scale,
-                                  cu_seqlens=cu_list, layout=w.layout, deterministic=det)
+                                  cu_seqlens=cu_list, layout=w.layout, deterministic=det,
+                                  window=window)
     torch.cuda.synchronize()
     assert binding.attn_fwd_status() == 0
     out = {"O": o, "LSE": lse, "dQ": dq, "dK": dk, "dV": dv}
@@ -66,12 +67,12 @@ def inputs_as_problems(x, w):
     return [problems(x[n], w, cu) for n in ("q", "k", "v", "dO")], cu
 
 
-def compare_full(x, w, g, pick=None):
+def compare_full(x, w, g, pick=None, window=None):
     """Full oracle on the problems in `pick` (all when None); returns error dict."""
     (q, k, v, dO), cu = inputs_as_problems(x, w)
     idx = list(range(len(q))) if pick is None else list(pick)
     sel = lambda lst: [lst[i] for i in idx]
-    r = oracle.backward(sel(q), sel(k), sel(v), sel(dO), w.causal, w.scale)
+    r = oracle.backward(sel(q), sel(k), sel(v), sel(dO), w.causal, w.scale, window=window)
     gp = {key: sel(problems(g[key], w, cu)) for key in ("O", "dQ", "dK", "dV")}
     gl = sel(lse_problems(g["LSE"], w, cu))
     cat = lambda a: np.concatenate([np.asarray(z).reshape(-1) for z in a])

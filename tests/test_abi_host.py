@@ -156,3 +156,20 @@ def test_step_host_scratch_formula(lib):
             2 * one + r256(H * 4), (B, H, T, dqk, dv, G, det)
     assert binding.attn_step_host_scratch_size(1, 4, 128, 96, 96) == 0
     assert binding.attn_step_host_scratch_size(1, 4, 128, 64, 64, -1) == 0
+
+
+def test_window_rejects(lib):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Tq=128, Tk=256, dqk=64, dv=64, causal=0,
+                window_left=16, window_right=0, scale=0.125, cu_seqlens=None, layout=0, stream=0)
+    bad = dict(args, window_left=-2)
+    assert binding.attn_fwd_window(**bad) == binding.ATTN_ERR_INVALID_ARG
+    bad = dict(args, window_right=-5)
+    assert binding.attn_fwd_window(**bad) == binding.ATTN_ERR_INVALID_ARG
+    more_q = dict(args, Tq=300)  # a window with more queries than keys
+    assert binding.attn_fwd_window(**more_q) == binding.ATTN_ERR_UNSUPPORTED
+    bargs = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, dq=A, dk=A, dv_out=A, B=1, H=2, Tq=300, Tk=256,
+                 dqk=64, dv=64, causal=0, window_left=-1, window_right=4, scale=0.125,
+                 cu_seqlens=None, layout=0, deterministic=0, workspace=A,
+                 workspace_bytes=1 << 30, stream=0)
+    assert binding.attn_bwd_window(**bargs) == binding.ATTN_ERR_UNSUPPORTED
+

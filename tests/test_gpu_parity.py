@@ -107,12 +107,55 @@ def test_causal_fewer_queries_than_keys(B, H, Tq, Tk, d, dv):
     dev = "cuda:0"
     q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
     o, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
+    assert binding.attn_fwd_status() == 0
+    need = binding.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, False, True)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
     for det in (False, True):
         dq, dk, dvv = binding.backward(q, k, v, o, dO, lse, causal=True, scale=w.scale,
-                                       deterministic=det)
+                                       deterministic=det, workspace=ws)
+        assert binding.attn_bwd_status(ws) == 0
         g = {"O": o.float().cpu(), "LSE": lse.cpu(), "dQ": dq.float().cpu(),
              "dK": dk.float().cpu(), "dV": dvv.float().cpu()}
         gc.assert_within(gc.compare_full(x, w, g), f"Tq={Tq} Tk={Tk} det={det}")
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,d,dv,causal,window", [
+    (1, 2, 700, 700, 64, 64, True, (200, -1)),      # causal local window
+    (1, 2, 700, 700, 128, 128, False, (100, 60)),   # two-sided band, edges inside tiles
+    (2, 2, 300, 300, 128, 128, False, (0, 0)),      # each query sees its own key only
+    (1, 2, 200, 900, 64, 64, False, (150, 10)),     # Tq < Tk: early keys seen by no query
+    (1, 1, 384, 384, 192, 128, True, (128, -1)),    # band edge on a tile boundary, d192
+    (1, 2, 520, 520, 128, 128, False, (-1, 100)),   # right bound only
+])
+def test_local_window(B, H, Tq, Tk, d, dv, causal, window):
+    """Local (sliding-window) attention against the oracle, fast and deterministic."""
+    g0 = torch.Generator().manual_seed(80 + Tq + (window[0] if window[0] > 0 else 0))
+    x = {"q": torch.randn(B, Tq, H, d, generator=g0).bfloat16(),
+         "k": torch.randn(B, Tk, H, d, generator=g0).bfloat16(),
+         "v": torch.randn(B, Tk, H, dv, generator=g0).bfloat16(),
+         "dO": torch.randn(B, Tq, H, dv, generator=g0).bfloat16()}
+    w = W("window", B, H, Tq, d, dv, causal)
+    dev = "cuda:0"
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o, lse = binding.forward(q, k, v, causal=causal, scale=w.scale, window=window)
+    assert binding.attn_fwd_status() == 0
+    need = binding.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, False, True)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    for det in (False, True):
+        dq, dk, dvv = binding.backward(q, k, v, o, dO, lse, causal=causal, scale=w.scale,
+                                       deterministic=det, window=window, workspace=ws)
+        assert binding.attn_bwd_status(ws) == 0
+        g = {"O": o.float().cpu(), "LSE": lse.cpu(), "dQ": dq.float().cpu(),
+             "dK": dk.float().cpu(), "dV": dvv.float().cpu()}
+        gc.assert_within(gc.compare_full(x, w, g, window=window),
+                         f"window={window} causal={causal} det={det}")
+
+
+def test_local_window_varlen():
+    w = W("varlen_window", 4, 2, 300, 128, 128, True, varlen=(300, 1, 257, 142))
+    x = syn.make_inputs(w, seed=81)
+    g = gc.run_gpu(x, w, window=(100, -1))
+    gc.assert_within(gc.compare_full(x, w, g, window=(100, -1)), "varlen window")
 
 
 # ---------------------------------------------------------------------------
