@@ -246,8 +246,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         return true;
       };
+      // descriptors of ring slot 0; slot s adds s * (slot bytes >> 4) to the
+      // start-address field (no carry: shared addresses stay below 2^18)
+      const uint64_t bK_0 = kmajor_base(sK), bV_0 = mnmajor_base(sV, 128);
       auto mma_S = [&](uint64_t bQ, uint32_t tS, uint64_t& sfull, uint32_t t) {
-        const uint64_t bK = kmajor_base(sK + (t % C::kKStages) * C::kKBytes);
+        const uint64_t bK = bK_0 + (uint64_t)((t % C::kKStages) * (C::kKBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
           mma_bf16(tS, bQ + kmajor_step(kk, 128), bK + kmajor_step(kk, 128), idS,
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(smem_u32(&sfull));
       };
       auto mma_PV = [&](uint32_t tS, uint32_t tO, uint32_t t, bool first) {  // A = P from TMEM
-        const uint64_t bV = mnmajor_base(sV + (t % C::kVStages) * C::kVBytes, 128);
+        const uint64_t bV = bV_0 + (uint64_t)((t % C::kVStages) * (C::kVBytes >> 4));
         mma_bf16_ts(tO, tS, bV, idO, first ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < kTile / 16; ++kk)
@@ -263,18 +266,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       const uint32_t tS0 = tmem + C::kTmemS, tS1 = tmem + C::kTmemS + 128;
       const uint32_t tO0 = tmem + C::kTmemO, tO1 = tmem + C::kTmemO + DV;
-      // one Q tile's step at kv tile j (ring index t): if j is in its range
-      // [lo, hi], wait for its P and do O += P V; then S of kv tile j+1 if that
-      // is in its range
+      // one Q tile's step at kv tile j (ring index t): when j is in its range,
+      // wait for its P and do O += P V (first / last of the range flagged);
+      // then S of kv tile j+1 when that is in its range
       auto step = [&](uint32_t tS, uint32_t tO, uint64_t bQ, uint64_t& pfull, uint64_t& sfull,
-                      uint64_t& odone, uint32_t& cnt, int j, int lo, int hi, uint32_t t) -> bool {
-        if (j >= lo && j <= hi) {
+                      uint64_t& odone, uint32_t& cnt, bool pv, bool first, bool last,
+                      bool s_next, uint32_t t) -> bool {
+        if (pv) {
           if (!W(pfull, cnt & 1)) return false;
-          mma_PV(tS, tO, t, j == lo);
-          if (j == hi) mma_commit(smem_u32(&odone));
+          mma_PV(tS, tO, t, first);
+          if (last) mma_commit(smem_u32(&odone));
           ++cnt;
         }
-        if (j + 1 >= lo && j + 1 <= hi) mma_S(bQ, tS, sfull, t + 1);
+        if (s_next) mma_S(bQ, tS, sfull, t + 1);
         return true;
       };
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
@@ -296,11 +300,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
           if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
             break;
-          if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0, j,
-                          lo0, hi0, t)))
+          // tile 0's range starts at lo0 and tile 1's ends at hi1 = lo0 + n - 1
+          if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
+                          j <= hi0, r == 0, j == hi0, j + 1 <= hi0, t)))
             break;
-          if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1, j,
-                          lo1, hi1, t)))
+          if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
+                          j >= lo1, j == lo1, !next, next && j + 1 >= lo1, t)))
             break;
           mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
           if (next) {
