@@ -628,10 +628,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_after();
         if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(20, gi);
         uint32_t pk[32];  // P^T of this thread's key row, 64 queries as bf16 pairs
-        // query columns below qmin are masked: all of them for a key past the
-        // sequence end, those before the key on the causal diagonal tile
-        // key kidx is visible to query q iff kidx - off - wr <= q <= kidx - off + wl:
-        // this group's visible query columns are [qmin, qmax)
+        // key kidx is visible to query q iff kidx - off - wr <= q <= kidx - off + wl
+        // (band bounds; -1 = open): this group's visible query columns are
+        // [qmin, qmax), none for a key past the sequence end
         const int qrel = kidx0 - kTile * i - grp * 64;  // kidx - (first query of the group)
         const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - sh.band_off - sh.wr)) : 0);
         const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - sh.band_off + sh.wl + 1)) : 64;

@@ -101,8 +101,7 @@ __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const 
   it.head = bh - it.seq * sh.H;
   it.Lq = sh.Tq;
   it.Lk = sh.Tk;
-  it.row0 = it.seq * sh.Tq;  // same for keys: fixed-length causal needs Tq == Tk,
-                             // non-causal keys use row0k below
+  it.row0 = it.seq * sh.Tq;  // query rows; the keys start at key_row0() (seq * Tk)
   it.tile_base = it.seq * sh.nq_tiles;
   return it;
 }
