@@ -55,12 +55,14 @@ def _open(path):
     P = ctypes.c_void_p
     I = ctypes.c_int
     D = ctypes.c_double
-    lib.oracle_forward.argtypes = [I, P, P, P, P, I, I, I, I, I, D, P, P, P, P, P, P, P]
+    lib.oracle_forward.argtypes = [I, P, P, P, P, I, I, I, I, I, P, I, I, I, D,
+                                   P, P, P, P, P, P, P]
     lib.oracle_forward.restype = I
-    lib.oracle_backward.argtypes = [I, I, P, P, P, P, I, I, I, I, I, D, P, P, P, P,
-                                    P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_backward.argtypes = [I, I, P, P, P, P, I, I, I, I, I, P, I, I, I, D,
+                                    P, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_backward.restype = I
-    lib.oracle_kv_rows.argtypes = [I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, I, P, P]
+    lib.oracle_kv_rows.argtypes = [I, I, I, I, I, I, I, P, I, I, I, D, P, P, P, P, P, P,
+                                   P, I, P, P]
     lib.oracle_kv_rows.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
@@ -128,11 +130,28 @@ def _window(window):
     return (-1 if wl is None else int(wl)), (-1 if wr is None else int(wr))
 
 
-def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None, window=None):
+def _blocks(block_mask, nprob, block):
+    """uint8 [nprob][nqb][nkb] block masks (a 2-D mask is shared by every
+    problem) and the ctypes arguments (pointer, nqb, nkb, block)."""
+    if block_mask is None:
+        return None, (None, 0, 0, 0)
+    m = np.asarray(block_mask)
+    if m.ndim == 2:
+        m = np.broadcast_to(m, (nprob,) + m.shape)
+    if m.ndim != 3 or m.shape[0] != nprob:
+        raise ValueError("block_mask must be [nqb][nkb] or [nprob][nqb][nkb]")
+    m = np.ascontiguousarray(m != 0, dtype=np.uint8)
+    return m, (_ptr(m), int(m.shape[1]), int(m.shape[2]), int(block))
+
+
+def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None, window=None,
+            block_mask=None, block: int = 128):
     """O, LSE (natural log) and, when dO is given, D_i = sum_j P_ij dP_ij.
 
     q: [nprob][Tq][dqk] (or list), k: [nprob][Tk][dqk], v: [nprob][Tk][dv].
     window: (left, right) local-attention bounds (see attn_oracle.c), or None.
+    block_mask: optional [nqb][nkb] or [nprob][nqb][nkb] array; key j is
+    visible to query i only where block_mask[i // block][j // block] != 0.
     Returns (O, LSE, D) with D None when dO is None.
     """
     lib = lib or _load()
@@ -142,8 +161,10 @@ def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None, window=None)
     LSE = np.zeros(nq)
     Dv = np.zeros(nq) if dO is not None else None
     wl, wr = _window(window)
+    keep, bm = _blocks(block_mask, pr.n, block)
     rc = lib.oracle_forward(pr.n, _ptr(pr.qrow0), _ptr(pr.Tq), _ptr(pr.krow0),
-                            _ptr(pr.Tk), pr.dqk, pr.dv, int(causal), wl, wr, float(scale),
+                            _ptr(pr.Tk), pr.dqk, pr.dv, int(causal), wl, wr, *bm,
+                            float(scale),
                             _ptr(pr.Q), _ptr(pr.K), _ptr(pr.V), _ptr(pr.dO),
                             _ptr(O), _ptr(LSE), _ptr(Dv))
     if rc != 0:
@@ -154,13 +175,15 @@ def forward(q, k, v, causal: bool, scale: float, dO=None, lib=None, window=None)
 
 
 def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
-             rows=None, want_matrices: bool = False, lib=None, window=None):
+             rows=None, want_matrices: bool = False, lib=None, window=None,
+             block_mask=None, block: int = 128):
     """Full backward by the chain rule of §2.1.
 
     mode "R": dS_i = P_i * (dP_i - <P_i, dP_i>) (row Jacobian-vector product);
     mode "E": dS_i = J_i dP_i with the explicit softmax Jacobian (§2.2 loop).
     rows: optional list (one per problem) of query-row index arrays; then only
     those rows' outputs are produced and dK/dV hold only their contributions.
+    window, block_mask, block: the visibility rule, as in forward().
     Returns a dict with dQ, dK, dV, O, LSE, D (and P, dS when
     want_matrices).  Arrays are stacked per problem when shapes agree.
     """
@@ -185,9 +208,10 @@ def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
         Pm = np.zeros(tot)
         dSm = np.zeros(tot)
     wl, wr = _window(window)
+    keep, bm = _blocks(block_mask, pr.n, block)
     rc = lib.oracle_backward(0 if mode == "R" else 1, pr.n, _ptr(pr.qrow0),
                              _ptr(pr.Tq), _ptr(pr.krow0), _ptr(pr.Tk), pr.dqk,
-                             pr.dv, int(causal), wl, wr, float(scale), _ptr(pr.Q),
+                             pr.dv, int(causal), wl, wr, *bm, float(scale), _ptr(pr.Q),
                              _ptr(pr.K), _ptr(pr.V), _ptr(pr.dO), _ptr(rows_arr),
                              _ptr(nrows), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(O),
                              _ptr(LSE), _ptr(Dv), _ptr(Pm), _ptr(dSm))
@@ -213,10 +237,12 @@ def backward(q, k, v, dO, causal: bool, scale: float, mode: str = "R",
     return out
 
 
-def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None, window=None):
+def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None, window=None,
+            block_mask=None, block: int = 128):
     """dK, dV at the listed key rows of ONE problem, given its LSE and D.
 
     q: [Tq][dqk], k: [Tk][dqk], v: [Tk][dv], dO: [Tq][dv], lse/D: [Tq].
+    block_mask: optional [nqb][nkb] block mask of this problem.
     Returns (dK_rows [nkeys][dqk], dV_rows [nkeys][dv]).
     """
     lib = lib or _load()
@@ -225,8 +251,9 @@ def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None, win
     dk = np.zeros((len(keys), q.shape[1]))
     dv = np.zeros((len(keys), v.shape[1]))
     wl, wr = _window(window)
+    keep, bm = _blocks(block_mask, 1, block)
     rc = lib.oracle_kv_rows(q.shape[0], k.shape[0], q.shape[1], v.shape[1],
-                            int(causal), wl, wr, float(scale), _ptr(q), _ptr(k), _ptr(v),
+                            int(causal), wl, wr, *bm, float(scale), _ptr(q), _ptr(k), _ptr(v),
                             _ptr(dO), _ptr(lse), _ptr(D), _ptr(keys), len(keys),
                             _ptr(dk), _ptr(dv))
     if rc != 0:
@@ -234,9 +261,11 @@ def kv_rows(q, k, v, dO, lse, D, keys, causal: bool, scale: float, lib=None, win
     return dk, dv
 
 
-def loss(q, k, v, dO, causal: bool, scale: float, lib=None, window=None) -> float:
+def loss(q, k, v, dO, causal: bool, scale: float, lib=None, window=None,
+         block_mask=None, block: int = 128) -> float:
     """Scalar L = sum(O * dO) whose gradient the backward returns."""
-    O, _, _ = forward(q, k, v, causal, scale, lib=lib, window=window)
+    O, _, _ = forward(q, k, v, causal, scale, lib=lib, window=window,
+                      block_mask=block_mask, block=block)
     if isinstance(O, list):
         return float(sum((o * d).sum() for o, d in zip(O, dO)))
     return float((O * np.asarray(dO)).sum())

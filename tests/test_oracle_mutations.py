@@ -30,6 +30,13 @@ def _pins(oracle, lib):
         r = oracle.backward(q, k, v, dO, causal, s, mode="E", want_matrices=True, lib=lib)
         res[f"rowsum_dS_causal{int(causal)}"] = bool(
             np.max(np.abs(r["dS"].sum(-1))) <= 1e-12 * np.linalg.norm(r["dS"]))
+    # block-sparse mask (asymmetric) against the autograd route
+    q, k, v, dO = _small(n=1, T=8, Tk=10, d=3, seed=5)
+    bm = np.array([[1, 1, 0], [0, 1, 1], [1, 0, 1]])  # not symmetric
+    g = oracle.backward(q, k, v, dO, False, s, block_mask=bm, block=4, lib=lib)
+    t = _torch_reference(q, k, v, dO, False, s, block_mask=bm, block=4)
+    res["autograd_block_mask"] = all(
+        rel_err(g[key], t[key]) <= 1e-10 for key in ("O", "dQ", "dK", "dV"))
     # last row: causal == non-causal
     q, k, v, dO = _small(n=1, T=6, d=3, seed=4)
     Oc, Lc, _ = oracle.forward(q, k, v, True, s, lib=lib)
@@ -53,7 +60,7 @@ def test_oracle_passes_every_pin(oracle_mod):
     assert all(res.values()), res
 
 
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7])
 def test_planted_mistake_is_caught(oracle_mod, plant):
     lib = oracle_mod.planted(plant)
     res = _pins(oracle_mod, lib)

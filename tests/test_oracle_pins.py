@@ -43,8 +43,11 @@ def _fd_grad(oracle, q, k, v, dO, causal, scale, which, idx, h=1e-6, lib=None, w
     return float(((np.asarray(Op) - np.asarray(Om)) * dO).sum() / (2 * h))
 
 
-def _torch_reference(q, k, v, dO, causal, scale, window=None):
-    """PyTorch CPU fp64 autograd of softmax(s Q K^T + mask) V (independent route)."""
+def _torch_reference(q, k, v, dO, causal, scale, window=None, block_mask=None, block=None):
+    """PyTorch CPU fp64 autograd of softmax(s Q K^T + mask) V (independent route).
+
+    block_mask: [nqb][nkb] array expanded to an element mask with a Kronecker
+    product (every block entry becomes a block x block square)."""
     qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
     kt = torch.tensor(k, dtype=torch.float64, requires_grad=True)
     vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
@@ -63,6 +66,10 @@ def _torch_reference(q, k, v, dO, causal, scale, window=None):
             keep &= torch.ones(Tq, Tk, dtype=torch.bool).tril(off + right)
         if left >= 0:
             keep &= torch.ones(Tq, Tk, dtype=torch.bool).triu(off - left)
+    if block_mask is not None:
+        bm = torch.tensor(np.asarray(block_mask) != 0, dtype=torch.float64)
+        dense = torch.kron(bm, torch.ones(block, block, dtype=torch.float64)) > 0
+        keep &= dense[:Tq, :Tk]
     if not bool(keep.all()):
         S = S.masked_fill(~keep, float("-inf"))
     P = torch.softmax(S, dim=-1)
@@ -465,3 +472,134 @@ def test_window_rejects_more_queries_than_keys(oracle_mod):
     q, k, v, dO = _small(n=1, T=9, d=3, seed=74, Tk=5)
     with pytest.raises(ValueError):
         oracle_mod.backward(q, k, v, dO, False, 0.5, window=(2, 2))
+
+
+# --------------------------------------------------------------------------
+# block-sparse masks: key j visible to query i only where the block pair
+# (i // block, j // block) is marked, intersected with the band
+# --------------------------------------------------------------------------
+BLOCK_CASES = [
+    # (Tq, Tk, block, causal, window, mask)  -- every row sees some key
+    (10, 13, 4, False, None, [[1, 0, 0, 1], [0, 1, 1, 0], [1, 1, 0, 0]]),
+    (12, 12, 4, True, None, [[1, 0, 0], [0, 1, 0], [1, 0, 1]]),
+    (9, 12, 3, False, (3, 1), [[0, 1, 1, 0], [1, 0, 1, 1], [0, 1, 0, 1]]),
+]
+
+
+@pytest.mark.parametrize("Tq,Tk,block,causal,window,mask", BLOCK_CASES)
+def test_block_mask_against_autograd_and_fd(oracle_mod, Tq, Tk, block, causal, window, mask):
+    """Block-sparse masks (asymmetric, ragged last blocks, combined with the
+    causal band or a window): the autograd route with the Kronecker-expanded
+    mask, and central differences of every entry."""
+    q, k, v, dO = _small(n=1, T=Tq, d=3, seed=80 + Tq, Tk=Tk)
+    s = 0.55
+    kw = dict(window=window, block_mask=mask, block=block)
+    g = oracle_mod.backward(q, k, v, dO, causal, s, **kw)
+    t = _torch_reference(q, k, v, dO, causal, s, **kw)
+    assert np.all(np.isfinite(t["LSE"]))  # the case has no empty row
+    for key in ("O", "dQ", "dK", "dV"):
+        assert rel_err(g[key], t[key]) <= 1e-12, key
+    assert float(np.max(np.abs(g["LSE"] - t["LSE"]))) <= 1e-12
+
+    def fd(which, idx, h=1e-6):
+        args = {"q": q, "k": k, "v": v}
+        plus = {kk: vv.copy() for kk, vv in args.items()}
+        minus = {kk: vv.copy() for kk, vv in args.items()}
+        plus[which][idx] += h
+        minus[which][idx] -= h
+        Lp = oracle_mod.loss(plus["q"], plus["k"], plus["v"], dO, causal, s, **kw)
+        Lm = oracle_mod.loss(minus["q"], minus["k"], minus["v"], dO, causal, s, **kw)
+        return (Lp - Lm) / (2 * h)
+
+    for which, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        ref = max(np.max(np.abs(grad)), 1e-30)
+        for idx in np.ndindex(*grad.shape):
+            assert abs(fd(which, idx) - grad[idx]) <= 1e-7 * ref, (which, idx)
+
+
+@pytest.mark.parametrize("causal,window", [(False, None), (True, None), (False, (2, 3))])
+def test_block_mask_of_ones_changes_nothing(oracle_mod, causal, window):
+    q, k, v, dO = _small(n=2, T=11, d=4, seed=90)
+    s = 0.5
+    plain = oracle_mod.backward(q, k, v, dO, causal, s, window=window)
+    ones = oracle_mod.backward(q, k, v, dO, causal, s, window=window,
+                               block_mask=np.ones((3, 3)), block=4)
+    for key in ("O", "LSE", "D", "dQ", "dK", "dV"):
+        np.testing.assert_array_equal(ones[key], plain[key])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_diagonal_mask_splits_into_independent_segments(oracle_mod, causal):
+    """With only the diagonal blocks marked, each block of queries attends to
+    its own block of keys alone: the result is that of separate problems."""
+    T, b = 24, 8
+    q, k, v, dO = _small(n=1, T=T, d=5, seed=91)
+    s = 0.4
+    g = oracle_mod.backward(q, k, v, dO, causal, s, block_mask=np.eye(3), block=b)
+    for seg in range(3):
+        sl = slice(seg * b, (seg + 1) * b)
+        ref = oracle_mod.backward(q[:, sl], k[:, sl], v[:, sl], dO[:, sl], causal, s)
+        for key in ("O", "LSE", "dQ", "dK", "dV"):
+            np.testing.assert_allclose(g[key][:, sl], ref[key], rtol=1e-13, atol=1e-15)
+
+
+def test_block_mask_rows_with_no_key(oracle_mod):
+    """A query block with no marked key block: O = 0, LSE = -inf, dQ = D = 0,
+    and dK / dV are those of the same problem without these queries."""
+    Tq, Tk, b = 24, 20, 8
+    mask = np.array([[1, 0, 1], [0, 1, 1], [0, 0, 0]])
+    q, k, v, dO = _small(n=1, T=Tq, d=4, seed=92, Tk=Tk)
+    s = 0.6
+    g = oracle_mod.backward(q, k, v, dO, False, s, block_mask=mask, block=b)
+    assert np.all(g["O"][0, 16:] == 0) and np.all(g["dQ"][0, 16:] == 0)
+    assert np.all(g["LSE"][0, 16:] == -np.inf) and np.all(g["D"][0, 16:] == 0)
+    assert np.all(np.isfinite(g["LSE"][0, :16]))
+    cut = oracle_mod.backward(q[:, :16], k, v, dO[:, :16], False, s, block_mask=mask[:2],
+                              block=b)
+    for key in ("dK", "dV"):
+        np.testing.assert_array_equal(g[key], cut[key])
+    for key in ("O", "LSE", "dQ"):
+        np.testing.assert_array_equal(g[key][:, :16], cut[key])
+    # the forward alone agrees
+    O, lse, D = oracle_mod.forward(q, k, v, False, s, dO=dO, block_mask=mask, block=b)
+    np.testing.assert_array_equal(O, g["O"])
+    np.testing.assert_array_equal(lse, g["LSE"])
+
+
+def test_block_mask_masks_exactly_the_marked_pairs(oracle_mod):
+    """P and dS vanish outside (marked blocks AND causal band); rows of P sum to
+    one wherever a row sees a key."""
+    T, b = 10, 3
+    mask = np.array([[1, 0, 1, 1], [1, 1, 0, 0], [0, 1, 1, 0], [1, 0, 0, 1]])
+    q, k, v, dO = _small(n=1, T=T, d=3, seed=93)
+    r = oracle_mod.backward(q, k, v, dO, True, 0.7, mode="E", want_matrices=True,
+                            block_mask=mask, block=b)
+    for i in range(T):
+        for j in range(T):
+            inside = j <= i and mask[i // b, j // b] != 0
+            assert (r["P"][0, i, j] > 0) == inside, (i, j)
+            if not inside:
+                assert r["dS"][0, i, j] == 0
+    sums = r["P"][0].sum(-1)
+    seen = np.array([any(j <= i and mask[i // b, j // b] for j in range(T)) for i in range(T)])
+    np.testing.assert_allclose(sums[seen], 1.0, rtol=1e-14)
+    assert np.all(sums[~seen] == 0)
+
+
+def test_block_mask_key_rows_match_full(oracle_mod):
+    q, k, v, dO = _small(n=1, T=12, d=4, seed=94, Tk=16)
+    mask = np.array([[1, 0, 0, 1], [0, 0, 0, 0], [1, 1, 0, 1]])  # one empty query block
+    kw = dict(block_mask=mask, block=4)
+    g = oracle_mod.backward(q, k, v, dO, False, 0.4, **kw)
+    _, lse, D = oracle_mod.forward(q, k, v, False, 0.4, dO=dO, **kw)
+    dk, dv = oracle_mod.kv_rows(q[0], k[0], v[0], dO[0], np.asarray(lse)[0], np.asarray(D)[0],
+                                np.arange(16), False, 0.4, **kw)
+    np.testing.assert_allclose(dk, g["dK"][0], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dv, g["dV"][0], rtol=1e-12, atol=1e-15)
+    assert np.all(dk[8:12] == 0) and np.all(dv[8:12] == 0)  # key block 2 is never marked
+
+
+def test_block_mask_must_cover_the_problem(oracle_mod):
+    q, k, v, dO = _small(n=1, T=9, d=3, seed=95)
+    with pytest.raises(ValueError):
+        oracle_mod.backward(q, k, v, dO, False, 0.5, block_mask=np.ones((2, 3)), block=4)
