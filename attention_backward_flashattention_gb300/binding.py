@@ -35,7 +35,9 @@ MAX_VARLEN_SEQS = 1024
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
             "attn_profile_main_kernel", "attn_bwd_noalloc", "attn_step_host_scratch_size",
-            "attn_step_host", "attn_step_host_status", "attn_fwd_window", "attn_bwd_window")
+            "attn_step_host", "attn_step_host_status", "attn_fwd_window", "attn_bwd_window",
+            "attn_fwd_blocksparse", "attn_bwd_blocksparse")
+BLOCK = 128  # rows per block of a block-sparse mask
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +68,12 @@ def load():
         lib.attn_bwd_window.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
                                         P, I, I, P, SZ, P]
         lib.attn_bwd_window.restype = I
+        lib.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, I, I, F,
+                                             P, I, P]
+        lib.attn_fwd_blocksparse.restype = I
+        lib.attn_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
+                                             P, I, I, F, P, I, I, P, SZ, P]
+        lib.attn_bwd_blocksparse.restype = I
         lib.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_size.restype = SZ
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P,
@@ -155,6 +163,44 @@ def attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, 
                                   int(causal), int(window_left), int(window_right),
                                   float(scale), cu.ptr, layout, int(deterministic),
                                   _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left,
+                         window_right, block_mask, mask_batches, mask_heads, scale,
+                         cu_seqlens=None, layout=LAYOUT_BTHD, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq,
+                                       Tk, dqk, dv, int(causal), int(window_left),
+                                       int(window_right), _ptr(block_mask), int(mask_batches),
+                                       int(mask_heads), float(scale), cu.ptr, layout,
+                                       _stream(stream))
+
+
+def attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
+                         window_left, window_right, block_mask, mask_batches, mask_heads, scale,
+                         cu_seqlens=None, layout=LAYOUT_BTHD, deterministic=False,
+                         workspace=None, workspace_bytes=0, stream=None) -> int:
+    cu = _HostInts(cu_seqlens)
+    return load().attn_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                       _ptr(dq), _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv,
+                                       int(causal), int(window_left), int(window_right),
+                                       _ptr(block_mask), int(mask_batches), int(mask_heads),
+                                       float(scale), cu.ptr, layout, int(deterministic),
+                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def _mask_dims(block_mask):
+    """(mask, mask_batches, mask_heads) of a [NQ][NK] or [Bm][Hm][NQ][NK] uint8
+    device tensor (None: no block mask)."""
+    if block_mask is None:
+        return None, 1, 1
+    if block_mask.dtype != torch.uint8 or not block_mask.is_contiguous():
+        raise ValueError("block_mask must be a contiguous uint8 tensor")
+    if block_mask.dim() == 2:
+        return block_mask, 1, 1
+    if block_mask.dim() != 4:
+        raise ValueError("block_mask must be [NQ][NK] or [Bm][Hm][NQ][NK]")
+    return block_mask, block_mask.shape[0], block_mask.shape[1]
 
 
 def attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen=False, deterministic=False) -> int:
@@ -264,9 +310,11 @@ def _dims(q, k, v, cu_seqlens, layout):
 
 
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BTHD,
-            with_lse=True, stream=None, window=None):
+            with_lse=True, stream=None, window=None, block_mask=None):
     """O (bf16, like q with v's head size) and LSE (fp32) or None.
-    window: (left, right) local-attention bounds (-1: open side), or None."""
+    window: (left, right) local-attention bounds (-1: open side), or None.
+    block_mask: device uint8 [NQ][NK] or [Bm][Hm][NQ][NK] (NQ, NK: blocks of
+    BLOCK rows), non-zero = the block pair takes part, or None."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
     o = torch.empty(q.shape[:-2] + (H, dv), dtype=torch.bfloat16, device=q.device)
@@ -275,8 +323,9 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BT
         lse = torch.empty((H, Tq) if cu_seqlens is not None else (B, H, Tq),
                           dtype=torch.float32, device=q.device)
     wl, wr = (-1, -1) if window is None else window
-    rc = attn_fwd_window(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, wl, wr, scale,
-                         cu_seqlens, layout, stream)
+    bm, mb, mh = _mask_dims(block_mask)
+    rc = attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, wl, wr, bm, mb, mh,
+                              scale, cu_seqlens, layout, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return o, lse
@@ -284,8 +333,9 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BT
 
 def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
              layout=LAYOUT_BTHD, deterministic=False, workspace=None, stream=None, out=None,
-             window=None):
-    """(dq, dk, dv) as bf16 tensors shaped like q, k, v (a packed buffer for layout 1)."""
+             window=None, block_mask=None):
+    """(dq, dk, dv) as bf16 tensors shaped like q, k, v (a packed buffer for layout 1).
+    window, block_mask: as in forward()."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
     if out is not None:
@@ -301,9 +351,10 @@ def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wl, wr = (-1, -1) if window is None else window
-    rc = attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, wl, wr,
-                         scale, cu_seqlens, layout, deterministic, workspace,
-                         workspace.numel() * workspace.element_size(), stream)
+    bm, mb, mh = _mask_dims(block_mask)
+    rc = attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, wl,
+                              wr, bm, mb, mh, scale, cu_seqlens, layout, deterministic, workspace,
+                              workspace.numel() * workspace.element_size(), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dvt

@@ -146,6 +146,29 @@ int qtiles_bound(int B, int Tq, bool varlen) {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// Block-mask fields of the kernels' shape (mask may be null).  Returns
+// ATTN_OK or ATTN_ERR_INVALID_ARG.
+int set_block_mask(SeqShape* sh, const unsigned char* mask, int mask_batches, int mask_heads,
+                   int B, int H, int Tq, int Tk, const int* cu) {
+  sh->blk = nullptr;
+  sh->blk_bstride = sh->blk_hstride = 0;
+  sh->blk_nk = 0;
+  if (mask == nullptr) return ATTN_OK;
+  if ((mask_batches != 1 && mask_batches != B) || (mask_heads != 1 && mask_heads != H))
+    return ATTN_ERR_INVALID_ARG;
+  int nq = cdiv(Tq, kTile), nk = cdiv(Tk, kTile);
+  if (cu != nullptr) {  // blocks of the longest sequence
+    int longest = 0;
+    for (int b = 0; b < B; ++b) longest = std::max(longest, cu[b + 1] - cu[b]);
+    nq = nk = cdiv(longest, kTile);
+  }
+  sh->blk = mask;
+  sh->blk_nk = nk;
+  sh->blk_hstride = mask_heads == 1 ? 0 : (int64_t)nq * nk;
+  sh->blk_bstride = mask_batches == 1 ? 0 : (int64_t)mask_heads * nq * nk;
+  return ATTN_OK;
+}
+
 // Host-side fault injection (tests only): added to every ordered-dQ wait
 // target of deterministic backward calls, so that the wait can never succeed.
 std::atomic<int> g_sem_bias{0};
@@ -196,6 +219,15 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
                     int H, int Tq, int Tk, int dqk, int dv, int causal, int window_left,
                     int window_right, float scale, const int* cu_seqlens, int layout,
                     void* stream) {
+  return attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left,
+                              window_right, nullptr, 1, 1, scale, cu_seqlens, layout, stream);
+}
+
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
+                         int window_left, int window_right, const unsigned char* block_mask,
+                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
+                         int layout, void* stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;  // running max assumes s > 0
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -229,6 +261,8 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
   L.sh.wl = window_left;
   L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = 0;
+  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens);
+  if (rc) return rc;
   if (varlen) {
     int n_items = 0, n_qt = 0;
     build_tables(cu_seqlens, B, H, kFwdRows, &tables, &n_items, &n_qt);
@@ -270,6 +304,18 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     int Tk, int dqk, int dv, int causal, int window_left, int window_right,
                     float scale, const int* cu_seqlens, int layout, int deterministic,
                     void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
+                              window_left, window_right, nullptr, 1, 1, scale, cu_seqlens, layout,
+                              deterministic, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv_out,
+                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
+                         int window_left, int window_right, const unsigned char* block_mask,
+                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
+                         int layout, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv_out || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -307,6 +353,8 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
   L.sh.wl = window_left;
   L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = deterministic ? 1 : 0;
+  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens);
+  if (rc) return rc;
   int n_qtiles;
   if (varlen) {
     int n_items = 0;

@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(256)
       // stored negated: the main kernel adds them (packed FP32 pairs have no
       // negated-operand form)
       ws.ndsum[g] = -part;
-      ws.nlse2[g] = -l * kLog2e;
+      // a row that saw no key (LSE = -inf, a block mask) keeps P = 0
+      ws.nlse2[g] = l == -INFINITY ? -INFINITY : -l * kLog2e;
     }
   }
   // padding rows of each sequence's last q-tile: P must come out as zero there
@@ -286,6 +287,24 @@ struct BwdCfg {
 // TMEM column of the packed P^T operand for MMA K-step kk (16 queries).
 __device__ __forceinline__ uint32_t p_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
+// The block mask's column of the item's kv tile (entry of q-tile i at
+// col[i * blk_nk]); null in the kernels built without block-mask support
+// (kMask = false), where every walk below reduces to i, i + 1, ...
+template <bool kMask>
+__device__ __forceinline__ const uint8_t* mask_col(const SeqShape& sh, const Item& it) {
+  if constexpr (!kMask) return nullptr;
+  return sh.blk + it.seq * sh.blk_bstride + it.head * sh.blk_hstride + it.tile;
+}
+
+// The first q-tile >= i, below i1, whose pair with the item's kv tile the
+// block mask keeps (i1 when there is none).  Every role of the main kernel
+// walks the same q-tiles with it.
+__device__ __forceinline__ int next_qtile(const SeqShape& sh, const uint8_t* col, int i, int i1) {
+  if (col != nullptr)
+    while (i < i1 && __ldg(col + (int64_t)i * sh.blk_nk) == 0) ++i;
+  return i;
+}
+
 constexpr int kMaxStages = 4;
 
 struct BwdBars {
@@ -298,6 +317,7 @@ struct BwdBars {
   uint64_t ds_free;     // the dK and dQ products are done reading dS^T
   uint64_t drain;
   int item_slot[2];
+  int q_last[kMaxStages];  // 1: the stage's q-tile is its item's last (written with q_full)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -317,7 +337,9 @@ struct MainArgs {
   SeqShape sh;
 };
 
-template <int DQK, int DV, typename Tables>
+// kMask: built with block-mask support (sh.blk non-null); the kernels without
+// it carry none of the mask's walks.
+template <int DQK, int DV, typename Tables, bool kMask>
 __global__ void __launch_bounds__(kMainThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -416,13 +438,19 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow);
         const int nq = cdiv(it.Lq, kTile);
         const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
-        for (int i = i0; i < i1; ++i, ++q_it) {
+        const uint8_t* col = mask_col<kMask>(sh, it);
+        for (int i = next_qtile(sh, col, i0, i1), inext; i < i1; i = inext, ++q_it) {
+          inext = next_qtile(sh, col, i + 1, i1);
           const uint32_t st = q_it % C::kStages;
           const uint32_t par = ((q_it / C::kStages) & 1) ^ 1;
           const int qrow = it.row0 + i * kTile;
           const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
           if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), par, ab))) break;
           ATTN_TRACE_EV(40, q_it);
+          // under a block mask the MMA issuer learns from this flag whether
+          // another q-tile follows (published by the arrive below, read after
+          // its wait on q_full)
+          if constexpr (kMask) bars->q_last[st] = inext >= i1 ? 1 : 0;
           const uint32_t qb = smem_u32(&bars->q_full[st]);
           mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
           for (int p = 0; p < C::kQPanels; ++p)
@@ -518,26 +546,37 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const Item it = decode_item(sh, tb, item, false);
         const int nq = cdiv(it.Lq, kTile);
         const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+        // Without a block mask the q-tiles are i0 .. i1-1.  With one, the
+        // producer's per-stage flag says whether a stage's q-tile is the
+        // item's last (read right after the stage's q_full wait, one step
+        // before it is needed, so that the load's latency is hidden).
+        const bool none = next_qtile(sh, mask_col<kMask>(sh, it), i0, i1) >= i1;
+        auto last_flag = [&](uint32_t st) {
+          return *static_cast<volatile int*>(&bars->q_last[st]) != 0;
+        };
         if (!(ok = W(bars->kv_full, k & 1))) break;
         // dK/dV accumulators of the previous item read out by the epilogue
         if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
-        if (i1 <= i0) {
-          // no query sees this kv tile (a local window): the epilogue writes
-          // zeros; nothing to compute
+        if (none) {
+          // no query sees this kv tile (a local window or a block mask): the
+          // epilogue writes zeros; nothing to compute
         } else if (!C::kSharedSdP) {
           // S and dP of the first q-tile; afterwards S_{i+1} is issued right
           // after dV_i so that P_{i+1} is computed while dK_i and dQ_i run.
           const uint32_t st0 = q_it % C::kStages;
           if (!(ok = W(bars->q_full[st0], (q_it / C::kStages) & 1))) break;
+          bool more_next = kMask ? !last_flag(st0) : true;  // kMask: another q-tile follows
           mma_S(st0);
           if (C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
           if (!(ok = W(bars->do_full[st0], (q_it / C::kStages) & 1))) break;
           mma_dP(st0);
-          for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
+          bool go = true;  // kMask: the previous q-tile was not the item's last
+          for (int i = i0; kMask ? go : i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;
             const uint32_t st1 = (q_it + 1) % C::kStages;
             const uint32_t par1 = ((q_it + 1) / C::kStages) & 1;
-            const bool first = (i == i0), more = (i + 1 < i1);
+            const bool first = (i == i0), more = kMask ? more_next : i + 1 < i1;
+            go = more;
             if (!(ok = W(bars->p_full, gi & 1))) break;
             ATTN_TRACE_EV(10, gi);
             mma_dV(st, first);
@@ -545,6 +584,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             if (more) {
               if (!(ok = W(bars->q_full[st1], par1))) break;
               ATTN_TRACE_EV(11, gi);
+              if constexpr (kMask) more_next = !last_flag(st1);
               mma_S(st1);
             }
             if (!(ok = W(bars->ds_half[0], gi & 1))) break;
@@ -570,11 +610,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
         } else {
           // S and dP share columns, and dQ covers them: one q-tile at a time
-          for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
+          bool go = true;  // kMask: the previous q-tile was not the item's last
+          for (int i = i0; kMask ? go : i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;
             const uint32_t par = (q_it / C::kStages) & 1;
             const bool first = (i == i0);
             if (!(ok = W(bars->q_full[st], par))) break;
+            if constexpr (kMask) go = !last_flag(st);
             if (gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
             mma_S(st);
             if (!(ok = W(bars->p_full, gi & 1))) break;
@@ -619,7 +661,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
       const int kidx0 = it.tile * kTile + r;  // this thread's key
       const bool key_ok = kidx0 < it.Lk;
-      for (int i = i0; i < i1; ++i, ++q_it, ++gi) {
+      const uint8_t* col = mask_col<kMask>(sh, it);
+      for (int i = next_qtile(sh, col, i0, i1); i < i1;
+           i = next_qtile(sh, col, i + 1, i1), ++q_it, ++gi) {
         const uint32_t st = q_it % C::kStages;
         const float* nlse2 = stat_f + st * (C::kStatBytes / 4) + grp * 64;  // -LSE * log2(e)
         const float* ndsum = nlse2 + kTile;                                  // -D
@@ -735,8 +779,27 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
       const int nk = cdiv(it.Lk, kTile);
-      const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
-      for (int i = i0; i < i1; ++i, ++gi) {
+      const int i1 = last_qtile(sh, it.tile, nq) + 1;
+      const uint8_t* col = mask_col<kMask>(sh, it);
+      const int ifirst = next_qtile(sh, col, first_qtile(sh, it.tile), i1);
+      for (int i = ifirst; i < i1; i = next_qtile(sh, col, i + 1, i1), ++gi) {
+        // deterministic order: contributions to q-tile i are added in
+        // descending kv-tile order.  The tile's word holds 1 + the kv tile
+        // that added to it last (0: none yet); this one waits for the
+        // contributor just above it: the next kv tile up within q-tile i's
+        // band (that the block mask keeps).
+        auto wait_target = [&]() {
+          const int last = last_kvtile(sh, i, nk);
+          int above = it.tile + 1;
+          if constexpr (kMask)
+            while (above <= last && !tile_on(sh, it, i, above)) ++above;
+          return (above <= last ? above + 1 : 0) + a.sem_bias;
+        };
+        // under a block mask the search reads the mask: done before the dQ
+        // row is loaded, while few registers are live
+        int target_m = 0;
+        if constexpr (kMask)
+          if (a.deterministic && wt == 0) target_m = wait_target();
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(30, gi);
@@ -753,10 +816,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
         float* acc = a.ws.dq_acc + g * (kTile * DQK);
         if (a.deterministic) {
-          // contributions to q-tile i are added in descending kv-tile order
           int* sem = a.ws.sem + g;
-          const int target = last_kvtile(sh, i, nk) - it.tile + a.sem_bias;
           if (wt == 0) {
+            const int target = kMask ? target_m : wait_target();
             const uint64_t t0 = globaltimer();
             while (ld_acquire_gpu(sem) != target) {
               // give up on our own limit, or as soon as any CTA has failed
@@ -780,7 +842,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           named_bar_sync(1, 128);
           if (wt == 0) {
             __threadfence();
-            red_release_gpu_add(a.ws.sem + g, 1);
+            st_release_gpu(a.ws.sem + g, it.tile + 1);
           }
         }
       }
@@ -796,7 +858,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + C::kTmemdK + c * 32, v);
         tmem_ld_wait();
-        if (i1 <= i0) {  // no query sees this kv tile: nothing was accumulated
+        if (ifirst >= i1) {  // no query sees this kv tile: nothing was accumulated
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
@@ -818,7 +880,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + C::kTmemdV + c * 32, v);
         tmem_ld_wait();
-        if (i1 <= i0) {
+        if (ifirst >= i1) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
@@ -927,7 +989,8 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
 #endif
     a.ws = L.ws;
     a.sh = L.sh;
-    auto* k = attn_bwd_main_kernel<DQK, DV, Tables>;
+    auto* k = L.sh.blk != nullptr ? attn_bwd_main_kernel<DQK, DV, Tables, true>
+                                  : attn_bwd_main_kernel<DQK, DV, Tables, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

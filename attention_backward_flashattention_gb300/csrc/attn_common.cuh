@@ -64,6 +64,13 @@ struct SeqShape {
   int band_off;
   int wl, wr;
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
+  // Block mask (null: every tile pair in the band takes part).  Byte
+  // [b][h][qt][kt] of a (mask batches, mask heads, q-tiles, kv-tiles) array;
+  // a zero byte drops the pair (query tile qt, key tile kt) of sequence b,
+  // head h.  A stride of 0 shares one mask over sequences or heads.
+  const uint8_t* blk;
+  int64_t blk_bstride, blk_hstride;  // bytes between sequences / heads
+  int blk_nk;                        // kv-tiles per mask row
 };
 
 struct Item {
@@ -155,6 +162,14 @@ __device__ __forceinline__ int last_qtile(const SeqShape& sh, int kt, int nq) {
   if (sh.wl < 0) return nq - 1;
   const int num = kt * kTile + kTile - 1 - sh.band_off + sh.wl;
   return num < 0 ? -1 : min(nq - 1, num / kTile);
+}
+
+// Whether the block mask keeps the tile pair (q-tile qt, kv-tile kt) of the
+// item's sequence and head (both tiles inside the sequence).
+__device__ __forceinline__ bool tile_on(const SeqShape& sh, const Item& it, int qt, int kt) {
+  return sh.blk == nullptr ||
+         __ldg(sh.blk + it.seq * sh.blk_bstride + it.head * sh.blk_hstride +
+               (int64_t)qt * sh.blk_nk + kt) != 0;
 }
 
 // First token row of the keys of a sequence (fixed-length Tk may differ from Tq).

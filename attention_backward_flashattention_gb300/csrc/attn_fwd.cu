@@ -125,7 +125,21 @@ __device__ __forceinline__ void kv_ranges(const SeqShape& sh, const Item& it, in
   lo1 = min(first_kvtile(sh, 2 * it.tile + 1), hi1);
 }
 
-template <int DQK, int DV, typename Tables>
+// Whether Q tile w (0, 1) of the item uses kv tile j: j lies in the tile's
+// band range [lo, hi] and the block mask keeps the pair.  With a block mask
+// (kMask) a Q tile wholly past the sequence end uses no kv tile at all.
+template <bool kMask>
+__device__ __forceinline__ bool kv_used(const SeqShape& sh, const Item& it, int w, int j, int lo,
+                                        int hi) {
+  if (j < lo || j > hi) return false;
+  if constexpr (!kMask) return true;
+  const int qt = 2 * it.tile + w;
+  return qt * kTile < it.Lq && tile_on(sh, it, qt, j);
+}
+
+// kMask: built with block-mask support (sh.blk non-null); the kernels without
+// it carry none of the mask's walks.
+template <int DQK, int DV, typename Tables, bool kMask>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -202,7 +216,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_load_3d(sQ + w * C::kQTileBytes + pnl * kPanelBytes, &tm_q, qf, pnl * 64, it.head,
                         it.row0 + it.tile * kFwdRows + w * kTile);
         const int krow0 = key_row0(sh, it);
-        for (int j = lo0; j <= hi1; ++j, ++kv_it) {  // every kv tile either Q tile sees
+        for (int j = lo0; j <= hi1; ++j) {  // every kv tile either Q tile uses
+          if (!kv_used<kMask>(sh, it, 0, j, lo0, hi0) && !kv_used<kMask>(sh, it, 1, j, lo1, hi1)) continue;
           const uint32_t sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           if (!(ok = mbar_wait(smem_u32(&bars->k_empty[sk]), ((kv_it / C::kKStages) & 1) ^ 1, ab)))
             break;
@@ -219,6 +234,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int pnl = 0; pnl < C::kVPanels; ++pnl)
             tma_load_3d(sV + sv * C::kVBytes + pnl * kPanelBytes, &tm_v, vf, pnl * 64, it.head,
                         krow0 + j * kTile);
+          ++kv_it;
         }
       }
       if (!ok) {
@@ -285,33 +301,59 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const Item it = decode_item(sh, tb, item, true);
         int lo0, hi0, lo1, hi1;
         kv_ranges(sh, it, lo0, hi0, lo1, hi1);
-        const int n = hi1 - lo0 + 1;  // kv tiles loaded for the item, from lo0
+        auto u0 = [&](int j) { return kv_used<kMask>(sh, it, 0, j, lo0, hi0); };
+        auto u1 = [&](int j) { return kv_used<kMask>(sh, it, 1, j, lo1, hi1); };
+        // the kv tiles loaded for the item (those either Q tile uses): their
+        // number n and each Q tile's first and last one.  Without a block
+        // mask they are lo0 .. hi1 (the two band ranges leave no gap).
+        int n = hi1 - lo0 + 1, f0 = lo0, l0 = hi0, f1 = lo1, l1 = hi1;
+        if constexpr (kMask) {
+          n = 0;
+          f0 = f1 = INT_MAX;
+          l0 = l1 = -1;
+          for (int j = lo0; j <= hi1; ++j) {
+            const bool a0 = u0(j), a1 = u1(j);
+            if (a0) { f0 = min(f0, j); l0 = j; }
+            if (a1) { f1 = min(f1, j); l1 = j; }
+            n += (a0 || a1) ? 1 : 0;
+          }
+        }
+        auto next_loaded = [&](int j) {
+          if constexpr (kMask)
+            while (j <= hi1 && !u0(j) && !u1(j)) ++j;
+          return j;
+        };
         if (!(ok = W(bars->q_full, item_iter & 1))) break;
-        // S of the first kv tile (tile 1 joins later when its band starts later)
+        if (n == 0) {  // the block mask drops every tile pair of the item
+          mma_commit(smem_u32(&bars->q_empty));
+          continue;
+        }
+        int j = next_loaded(lo0);
+        // S of the first kv tile, for each Q tile that uses it
         if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
-        mma_S(bQ0, tS0, bars->s_full[0], kv_it);
-        if (lo1 == lo0) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
+        if (u0(j)) mma_S(bQ0, tS0, bars->s_full[0], kv_it);
+        if (u1(j)) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
         mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
         if (n == 1) mma_commit(smem_u32(&bars->q_empty));
         for (int r = 0; ok && r < n; ++r) {
-          const int j = lo0 + r;
           const uint32_t t = kv_it + r;
           const bool next = r + 1 < n;
+          const int jn = next ? next_loaded(j + 1) : hi1 + 1;  // the next loaded kv tile
           if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
           if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
             break;
-          // tile 0's range starts at lo0 and tile 1's ends at hi1 = lo0 + n - 1
           if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
-                          j <= hi0, r == 0, j == hi0, j + 1 <= hi0, t)))
+                          u0(j), j == f0, j == l0, next && u0(jn), t)))
             break;
           if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
-                          j >= lo1, j == lo1, !next, next && j + 1 >= lo1, t)))
+                          u1(j), j == f1, j == l1, next && u1(jn), t)))
             break;
           mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
           if (next) {
             mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
             if (r + 2 == n) mma_commit(smem_u32(&bars->q_empty));  // after the last S
           }
+          j = jn;
         }
         if (!ok) break;
         kv_it += n;
@@ -340,7 +382,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int qt = 2 * it.tile + w;           // q-tile index within the sequence
       const int qidx = qt * kTile + r;
       float m = -INFINITY, l = 0.f;
-      for (int j = jlo; j <= jhi; ++j, ++cnt) {
+      bool started = false;  // this Q tile has had a kv tile
+      for (int j = jlo; j <= jhi; ++j) {
+        if (kMask && !kv_used<kMask>(sh, it, w, j, jlo, jhi)) continue;
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full[w]), cnt & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[4][32];
@@ -395,7 +439,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float alpha = resc ? ex2(m - m_use) : 1.0f;
         uint32_t pk0[32], pk1[32];  // P as bf16 pairs: keys 0-63, 64-127
         const float rowsum = softmax_exp(sr, scale_log2, m_use, pk0, pk1);
-        if (j > jlo && __any_sync(0xffffffffu, resc)) {
+        if ((kMask ? started : j > jlo) && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t ov[32];
@@ -415,16 +459,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[w]));
+        started = true;
+        ++cnt;
       }
       if (!ok) break;
-      // epilogue: O / l and the log-sum-exp
+      const bool valid = qidx < it.Lq;
+      __nv_bfloat16* orow =
+          out + (int64_t)(it.row0 + qidx) * o_row_stride + (int64_t)it.head * DV;
+      auto lse_at = [&]() {
+        return (int64_t)it.head * lse_head_stride +
+               (sh.varlen ? (int64_t)it.row0 : (int64_t)it.seq * lse_seq_stride) + qidx;
+      };
+      if (kMask && !started) {
+        // the block mask drops every kv tile of this Q tile: its rows see no
+        // key (empty sums): O = 0, LSE = -inf
+        if (valid) {
+#pragma unroll 1
+          for (int c = 0; c < DV / 8; ++c)
+            *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+          if (lse != nullptr) lse[lse_at()] = -INFINITY;
+        }
+        continue;
+      }
+      // epilogue: O / l and the log-sum-exp (under a block mask a row can have
+      // seen no key: l = 0, O = 0 and LSE = -inf)
       if (!(ok = mbar_wait_warp(smem_u32(&bars->o_done[w]), items_done & 1, ab))) break;
       ++items_done;
       tc_fence_after();
-      const bool valid = qidx < it.Lq;
-      const float inv_l = 1.0f / l;
-      __nv_bfloat16* orow =
-          out + (int64_t)(it.row0 + qidx) * o_row_stride + (int64_t)it.head * DV;
+      const bool no_key = kMask && !(l > 0.f);
+      const float inv_l = no_key ? 0.f : 1.0f / l;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t ov[32];
@@ -443,11 +506,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       tc_fence_before();
-      if (lse != nullptr && valid) {
-        const int64_t base = sh.varlen ? (int64_t)it.row0 : (int64_t)it.seq * lse_seq_stride;
-        lse[(int64_t)it.head * lse_head_stride + base + qidx] =
-            (m + log2f(l)) * 0.69314718055994530942f;
-      }
+      if (lse != nullptr && valid)
+        lse[lse_at()] = no_key ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
 
@@ -468,7 +528,8 @@ cudaError_t launch_typed(const FwdLaunch& L) {
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = L.stream;
   if (L.tables) {
-    auto* k = attn_fwd_kernel<DQK, DV, VarlenTables>;
+    auto* k = L.sh.blk != nullptr ? attn_fwd_kernel<DQK, DV, VarlenTables, true>
+                                  : attn_fwd_kernel<DQK, DV, VarlenTables, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v,
@@ -476,7 +537,8 @@ cudaError_t launch_typed(const FwdLaunch& L) {
                               L.lse_head_stride, L.lse_seq_stride, L.scale_log2, L.status, L.sh,
                               *L.tables);
   }
-  auto* k = attn_fwd_kernel<DQK, DV, NoTables>;
+  auto* k = L.sh.blk != nullptr ? attn_fwd_kernel<DQK, DV, NoTables, true>
+                                : attn_fwd_kernel<DQK, DV, NoTables, false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, reinterpret_cast<__nv_bfloat16*>(L.o),

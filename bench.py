@@ -396,6 +396,114 @@ def run_fwd_only(args, rank, world):
     }
 
 
+def block_sparse_mask(w, density, seed=0):
+    """Seeded random block mask of workload `w`, one per head: each pair of
+    128-row blocks kept with probability `density`, the diagonal always kept
+    (every query then sees at least its own block).  uint8 [1][H][n][n]."""
+    n = -(-w.T // 128)
+    m = (np.random.default_rng(seed).random((1, w.H, n, n)) < density).astype(np.uint8)
+    m[..., np.arange(n), np.arange(n)] = 1
+    return m
+
+
+def visible_pairs(w, mask):
+    """(query, key) pairs that the kept blocks and the causal band leave, summed
+    over heads and batch (the FLOP count's pair term; T a multiple of 128)."""
+    n = mask.shape[-1]
+    qt, kt = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    per_pair = np.full((n, n), 128.0 * 128.0)
+    if w.causal:
+        per_pair = np.where(kt < qt, 128.0 * 128.0, np.where(kt == qt, 128.0 * 129.0 / 2, 0.0))
+    return w.B * float((mask.astype(np.float64) * per_pair).sum())
+
+
+def run_block_sparse(args, rank, world):
+    """Forward + backward of the workload under a random block mask of the
+    given density (`--block-density`): TFLOP/s over the visible pairs only.
+    A separate measurement (not the headline line)."""
+    from attention_backward_flashattention_gb300 import binding
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    if w.T % 128:
+        raise ValueError("block-sparse bench wants T a multiple of 128")
+    x = syn.make_inputs(w)
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    mask = block_sparse_mask(w, args.block_density, seed=rank)
+    bm = torch.from_numpy(mask).to(dev)
+    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
+    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    dq, dk, dvt = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = binding.attn_bwd_workspace_size(B, H, T, T, dqk, dv, False, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    wl, wr = -1, -1
+
+    def fwd():
+        rc = binding.attn_fwd_blocksparse(q, k, v, o, lse, B, H, T, T, dqk, dv, w.causal, wl, wr,
+                                          bm, 1, H, w.scale, None, 0, stream)
+        assert rc == 0, rc
+
+    def bwd():
+        rc = binding.attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dvt, B, H, T, T, dqk, dv,
+                                          w.causal, wl, wr, bm, 1, H, w.scale, None, 0, False, ws,
+                                          need, stream)
+        assert rc == 0, rc
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    K = args.steps
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+    for s_ in range(K):  # the inputs (> L2) are re-read from HBM every step
+        ev[3 * s_].record(stream)
+        fwd()
+        ev[3 * s_ + 1].record(stream)
+        bwd()
+        ev[3 * s_ + 2].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if rank == 0 else None
+    if binding.attn_fwd_status() != 0 or binding.attn_bwd_status(ws) != 0:
+        raise RuntimeError("device status error in the timed region")
+    fwd_ms = sum(ev[3 * s_].elapsed_time(ev[3 * s_ + 1]) for s_ in range(K))
+    bwd_ms = sum(ev[3 * s_ + 1].elapsed_time(ev[3 * s_ + 2]) for s_ in range(K))
+    fwd_ms, bwd_ms = max_over_ranks([fwd_ms, bwd_ms], world, dev)
+    if rank != 0:
+        return None
+    pairs = visible_pairs(w, mask)
+    bwd_flops = 2.0 * pairs * (3 * dqk + 2 * dv)
+    fwd_flops = 2.0 * pairs * (dqk + dv)
+    peaks = _peaks()
+    per = bwd_flops / (bwd_ms / K * 1e-3) / 1e12
+    kept = float(mask.mean())
+    return {
+        "metric": "attn bwd TFLOP/s (bf16, block-sparse, visible pairs only)",
+        "value": job_tflops(bwd_flops, world, K, bwd_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": bwd_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": _config(w, {"block_mask": f"random per head, density {args.block_density} "
+                                            f"(diagonal kept; {kept:.3f} of block pairs kept)",
+                              "dense_bwd_flops": w.bwd_flops()}),
+        "fwd_tflops": job_tflops(fwd_flops, world, K, fwd_ms * 1e-3), "fwd_ms": fwd_ms / K,
+        "roofline": {"kernel": "attn_bwd (pre + main + convert)", "bound": "tensor",
+                     "achieved": per, "peak": peaks["bf16_sustained"], "unit": UNIT,
+                     "frac": per / peaks["bf16_sustained"], "traffic": None,
+                     "algorithmic_flops_per_launch": bwd_flops},
+        "gpu_launches": 4 * K, "clocks": clocks,
+    }
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -443,6 +551,8 @@ def main():
                     help="compute streams of the e2e pipeline")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the inference-mode forward (lse=NULL) instead of the step")
+    ap.add_argument("--block-density", type=float, default=0.0,
+                    help="time forward + backward under a random block mask of this density")
     args = ap.parse_args()
     WORKLOAD = syn.ALL[args.workload]
     if WORKLOAD.varlen or WORKLOAD.layout != syn.LAYOUT_BTHD:
@@ -462,7 +572,12 @@ def main():
             build_mod.build()
         if world > 1:
             torch.distributed.barrier()
-        line = run_fwd_only(args, rank, world) if args.fwd_only else run_ours(args, rank, world)
+        if args.block_density > 0:
+            line = run_block_sparse(args, rank, world)
+        elif args.fwd_only:
+            line = run_fwd_only(args, rank, world)
+        else:
+            line = run_ours(args, rank, world)
     else:
         line = run_reference(args, rank, world)
     if line is not None:

@@ -79,6 +79,7 @@ extern "C" {
 #define ATTN_LAYOUT_BTHD 0
 #define ATTN_LAYOUT_PACKED_QKV 1
 #define ATTN_MAX_VARLEN_SEQS 1024
+#define ATTN_BLOCK 128 /* rows per block of a block-sparse mask (the kernels' tile) */
 
 /*
  * Forward: O and (unless lse == NULL, inference mode) LSE.
@@ -146,6 +147,43 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Block-sparse attention: as attn_fwd_window, and in addition key j is visible
+ * to query i only where the block mask marks the pair of blocks
+ * (i / ATTN_BLOCK, j / ATTN_BLOCK) with a non-zero byte.  The block-sparse
+ * mask module of "深度学习反向传播优化：2-CTA MMA模式与内存访问优化" §5.1-5.2
+ * (FlexAttention and block-sparse variants built from the same kernels by a
+ * mask module alone): the kernels skip every tile pair the mask drops.
+ *   block_mask: DEVICE pointer to uint8 [mask_batches][mask_heads][NQ][NK],
+ *     C order, read only, owned by the caller, unchanged until the call's work
+ *     on `stream` is done.  NQ = ceil(Tq / ATTN_BLOCK), NK = ceil(Tk /
+ *     ATTN_BLOCK); for variable-length batches NQ = NK = ceil(longest sequence
+ *     / ATTN_BLOCK), and sequence b uses its own block coordinates (entries
+ *     past its end are not read).  mask_batches is 1 (one mask for every
+ *     sequence) or B; mask_heads is 1 or H.  NULL: attn_fwd_window.
+ * A query row that sees no key gets O = 0 and LSE = -inf (and, in
+ * attn_bwd_blocksparse, dQ = 0; it adds nothing to dK or dV).  Returns
+ * ATTN_ERR_INVALID_ARG for other mask_batches / mask_heads values.
+ */
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
+                         int window_left, int window_right, const unsigned char* block_mask,
+                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
+                         int layout, void* stream);
+
+/*
+ * Backward of attn_fwd_blocksparse (same mask arguments; lse from that
+ * forward).  Workspace as for attn_bwd.  Deterministic mode adds the dQ
+ * contributions of the kept key tiles in descending key-tile order.
+ */
+int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv_out,
+                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
+                         int window_left, int window_right, const unsigned char* block_mask,
+                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
+                         int layout, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Backward for callers that cannot allocate device memory (a plugin whose host
  * framework owns all device memory, or a loop where a device-synchronising
  * cudaMalloc is not allowed).  Same arguments and results as attn_bwd, minus
@@ -189,8 +227,9 @@ int attn_profile_main_kernel(void* event_start, void* event_stop);
 /*
  * Test hook (host-side fault injection; 0 = normal operation): every ordered
  * dQ wait of later deterministic attn_bwd calls in this process waits for a
- * semaphore value `bias` higher than the one that will come, so the bounded
- * wait gives up and attn_bwd_status() reports ATTN_ERR_TIMEOUT.  The kernels
+ * semaphore value `bias` higher than the one that will come (a bias above the
+ * number of key tiles can never be met), so the bounded wait gives up and
+ * attn_bwd_status() reports ATTN_ERR_TIMEOUT.  The kernels
  * stop, free their tensor memory and leave the CUDA context usable.  No
  * counterpart on the pages (whose printed spin-wait, §3.2 of "深度学习反向传播
  * 优化：2-CTA MMA模式与内存访问优化", has no bound).

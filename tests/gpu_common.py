@@ -67,19 +67,31 @@ def inputs_as_problems(x, w):
     return [problems(x[n], w, cu) for n in ("q", "k", "v", "dO")], cu
 
 
-def compare_full(x, w, g, pick=None, window=None):
-    """Full oracle on the problems in `pick` (all when None); returns error dict."""
+def compare_full(x, w, g, pick=None, window=None, block_mask=None):
+    """Full oracle on the problems in `pick` (all when None); returns error dict.
+
+    block_mask: optional [n_problems][NQ][NK] array (problem order as in
+    problems()), blocks of binding.BLOCK rows.  Rows the oracle gives LSE =
+    -inf (no visible key) must be -inf on the GPU too; the LSE error is taken
+    over the other rows."""
     (q, k, v, dO), cu = inputs_as_problems(x, w)
     idx = list(range(len(q))) if pick is None else list(pick)
     sel = lambda lst: [lst[i] for i in idx]
-    r = oracle.backward(sel(q), sel(k), sel(v), sel(dO), w.causal, w.scale, window=window)
+    bm = None if block_mask is None else np.asarray(block_mask)[idx]
+    r = oracle.backward(sel(q), sel(k), sel(v), sel(dO), w.causal, w.scale, window=window,
+                        block_mask=bm, block=binding.BLOCK)
     gp = {key: sel(problems(g[key], w, cu)) for key in ("O", "dQ", "dK", "dV")}
     gl = sel(lse_problems(g["LSE"], w, cu))
     cat = lambda a: np.concatenate([np.asarray(z).reshape(-1) for z in a])
     err = {key: rel_err(cat(gp[key]), cat(r[key] if isinstance(r[key], list) else list(r[key])))
            for key in ("O", "dQ", "dK", "dV")}
-    ref_lse = r["LSE"] if isinstance(r["LSE"], list) else list(r["LSE"])
-    err["LSE"] = max_abs(cat(gl), cat(ref_lse))
+    ref_lse = cat(r["LSE"] if isinstance(r["LSE"], list) else list(r["LSE"]))
+    got_lse = cat(gl)
+    empty = np.isneginf(ref_lse)
+    if not np.array_equal(np.isneginf(got_lse), empty):
+        err["LSE"] = float("inf")
+    else:
+        err["LSE"] = max_abs(got_lse[~empty], ref_lse[~empty]) if (~empty).any() else 0.0
     return err
 
 
