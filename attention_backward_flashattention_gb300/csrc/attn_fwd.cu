@@ -108,8 +108,17 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  // block mask only, written by the producer before the matching arrive:
+  int q_none;       // 1: the item loads no kv tile (with q_full)
+  int kv_flags[4];  // per K stage (with k_full): kKvUse0 | kKvUse1 | kKvFirst0 | ...
 };
 static_assert(sizeof(FwdBars) <= 512, "barrier block size");
+
+// kv_flags bits: which Q tiles use the stage's kv tile, whether it is a Q
+// tile's first or last in the visiting order, and whether it is the item's
+// last loaded kv tile.
+constexpr int kKvUse0 = 1, kKvUse1 = 2, kKvFirst0 = 4, kKvLast0 = 8, kKvFirst1 = 16,
+              kKvLast1 = 32, kKvItemLast = 64;
 
 // kv-tile ranges [lo_w, hi_w] of the two Q tiles of an item (the band's tiles;
 // lo0 <= lo1 and hi0 <= hi1, and the two ranges leave no gap between them).
@@ -135,6 +144,46 @@ __device__ __forceinline__ bool kv_used(const SeqShape& sh, const Item& it, int 
   if constexpr (!kMask) return true;
   const int qt = 2 * it.tile + w;
   return qt * kTile < it.Lq && tile_on(sh, it, qt, j);
+}
+
+// The order in which a block-masked item visits its kv tiles: first those
+// both Q tiles keep (ascending), then alternately one that only Q tile 0
+// keeps and one that only Q tile 1 keeps (each ascending).  Consecutive steps
+// then belong to different Q tiles, so each softmax warpgroup overlaps the
+// other tile's MMAs, as in the dense kernel; the online softmax does not
+// depend on the order of the kv tiles.
+struct MaskOrder {
+  int phase, c0, c1, turn;  // phase 0: tiles both keep; c0 / c1: scan positions
+};
+
+// The next kv tile in MaskOrder, or hi1 + 1 when none is left; `who` gets
+// the Q tiles that use it (bit 0: tile 0, bit 1: tile 1).
+__device__ __forceinline__ int mask_order_next(MaskOrder& o, const SeqShape& sh, const Item& it,
+                                               int lo0, int hi0, int lo1, int hi1, int& who) {
+  const int end = hi1 + 1;
+  if (o.phase == 0) {
+    while (o.c0 < end && !(kv_used<true>(sh, it, 0, o.c0, lo0, hi0) &&
+                           kv_used<true>(sh, it, 1, o.c0, lo1, hi1)))
+      ++o.c0;
+    who = 3;
+    if (o.c0 < end) return o.c0++;
+    o.phase = 1;
+    o.c0 = o.c1 = lo0;
+  }
+  for (int k = 0; k < 2; ++k) {  // this turn's Q tile; the other once that one has no tile left
+    const int w = o.turn ^ k;
+    int c = w ? o.c1 : o.c0;
+    while (c < end && !(kv_used<true>(sh, it, w, c, w ? lo1 : lo0, w ? hi1 : hi0) &&
+                        !kv_used<true>(sh, it, w ^ 1, c, w ? lo0 : lo1, w ? hi0 : hi1)))
+      ++c;
+    if (w) o.c1 = c + 1; else o.c0 = c + 1;
+    if (c < end) {
+      o.turn = w ^ 1;
+      who = 1 << w;
+      return c;
+    }
+  }
+  return end;
 }
 
 // kMask: built with block-mask support (sh.blk non-null); the kernels without
@@ -207,7 +256,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const Item it = decode_item(sh, tb, item, true);
         int lo0, hi0, lo1, hi1;
         kv_ranges(sh, it, lo0, hi0, lo1, hi1);
+        // block mask: how many kv tiles each Q tile uses and how many load
+        int tot0 = 0, tot1 = 0, nload = 0;
+        if constexpr (kMask) {
+          for (int j = lo0; j <= hi1; ++j) {
+            const bool a0 = kv_used<kMask>(sh, it, 0, j, lo0, hi0);
+            const bool a1 = kv_used<kMask>(sh, it, 1, j, lo1, hi1);
+            tot0 += a0 ? 1 : 0;
+            tot1 += a1 ? 1 : 0;
+            nload += (a0 || a1) ? 1 : 0;
+          }
+        }
         if (!(ok = mbar_wait(smem_u32(&bars->q_empty), (item_iter & 1) ^ 1, ab))) break;
+        if constexpr (kMask) bars->q_none = nload == 0 ? 1 : 0;
         const uint32_t qf = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qf, C::kQBytes);
         q_issued = item_iter + 1;
@@ -216,11 +277,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_load_3d(sQ + w * C::kQTileBytes + pnl * kPanelBytes, &tm_q, qf, pnl * 64, it.head,
                         it.row0 + it.tile * kFwdRows + w * kTile);
         const int krow0 = key_row0(sh, it);
-        for (int j = lo0; j <= hi1; ++j) {  // every kv tile either Q tile uses
-          if (!kv_used<kMask>(sh, it, 0, j, lo0, hi0) && !kv_used<kMask>(sh, it, 1, j, lo1, hi1)) continue;
+        // every kv tile either Q tile uses: lo0 .. hi1, or MaskOrder's tiles
+        MaskOrder ord{0, lo0, lo0, 0};
+        int who = 3, k0 = 0, k1 = 0, r = 0;
+        for (int j = kMask ? mask_order_next(ord, sh, it, lo0, hi0, lo1, hi1, who) : lo0; j <= hi1;
+             j = kMask ? mask_order_next(ord, sh, it, lo0, hi0, lo1, hi1, who) : j + 1) {
           const uint32_t sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           if (!(ok = mbar_wait(smem_u32(&bars->k_empty[sk]), ((kv_it / C::kKStages) & 1) ^ 1, ab)))
             break;
+          if constexpr (kMask) {  // the MMA issuer's step flags for this kv tile
+            int f = who;
+            if ((who & 1) && k0 == 0) f |= kKvFirst0;
+            if ((who & 1) && k0 + 1 == tot0) f |= kKvLast0;
+            if ((who & 2) && k1 == 0) f |= kKvFirst1;
+            if ((who & 2) && k1 + 1 == tot1) f |= kKvLast1;
+            if (r + 1 == nload) f |= kKvItemLast;
+            k0 += who & 1;
+            k1 += (who >> 1) & 1;
+            ++r;
+            bars->kv_flags[sk] = f;
+          }
           const uint32_t kf = smem_u32(&bars->k_full[sk]);
           mbar_arrive_expect_tx(kf, C::kKBytes);
           for (int pnl = 0; pnl < C::kQPanels; ++pnl)
@@ -297,66 +373,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (s_next) mma_S(bQ, tS, sfull, t + 1);
         return true;
       };
+      auto flag = [&](const int& v) { return *static_cast<const volatile int*>(&v); };
       for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
         const Item it = decode_item(sh, tb, item, true);
         int lo0, hi0, lo1, hi1;
         kv_ranges(sh, it, lo0, hi0, lo1, hi1);
-        auto u0 = [&](int j) { return kv_used<kMask>(sh, it, 0, j, lo0, hi0); };
-        auto u1 = [&](int j) { return kv_used<kMask>(sh, it, 1, j, lo1, hi1); };
-        // the kv tiles loaded for the item (those either Q tile uses): their
-        // number n and each Q tile's first and last one.  Without a block
-        // mask they are lo0 .. hi1 (the two band ranges leave no gap).
-        int n = hi1 - lo0 + 1, f0 = lo0, l0 = hi0, f1 = lo1, l1 = hi1;
-        if constexpr (kMask) {
-          n = 0;
-          f0 = f1 = INT_MAX;
-          l0 = l1 = -1;
-          for (int j = lo0; j <= hi1; ++j) {
-            const bool a0 = u0(j), a1 = u1(j);
-            if (a0) { f0 = min(f0, j); l0 = j; }
-            if (a1) { f1 = min(f1, j); l1 = j; }
-            n += (a0 || a1) ? 1 : 0;
-          }
-        }
-        auto next_loaded = [&](int j) {
-          if constexpr (kMask)
-            while (j <= hi1 && !u0(j) && !u1(j)) ++j;
-          return j;
-        };
         if (!(ok = W(bars->q_full, item_iter & 1))) break;
-        if (n == 0) {  // the block mask drops every tile pair of the item
-          mma_commit(smem_u32(&bars->q_empty));
-          continue;
-        }
-        int j = next_loaded(lo0);
-        // S of the first kv tile, for each Q tile that uses it
-        if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
-        if (u0(j)) mma_S(bQ0, tS0, bars->s_full[0], kv_it);
-        if (u1(j)) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
-        mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
-        if (n == 1) mma_commit(smem_u32(&bars->q_empty));
-        for (int r = 0; ok && r < n; ++r) {
-          const uint32_t t = kv_it + r;
-          const bool next = r + 1 < n;
-          const int jn = next ? next_loaded(j + 1) : hi1 + 1;  // the next loaded kv tile
-          if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
-          if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
-            break;
-          if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
-                          u0(j), j == f0, j == l0, next && u0(jn), t)))
-            break;
-          if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
-                          u1(j), j == f1, j == l1, next && u1(jn), t)))
-            break;
-          mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
-          if (next) {
-            mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
-            if (r + 2 == n) mma_commit(smem_u32(&bars->q_empty));  // after the last S
+        if constexpr (kMask) {
+          // block mask: the kv tiles come in MaskOrder; the producer's flags
+          // (read after the waits that publish them) say which Q tiles use
+          // each, its place among each Q tile's tiles, and the item's end
+          if (flag(bars->q_none)) {  // the mask drops every tile pair of the item
+            mma_commit(smem_u32(&bars->q_empty));
+            continue;
           }
-          j = jn;
+          uint32_t t = kv_it;
+          if (!(ok = W(bars->k_full[t % C::kKStages], (t / C::kKStages) & 1))) break;
+          int f = flag(bars->kv_flags[t % C::kKStages]);
+          if (f & kKvUse0) mma_S(bQ0, tS0, bars->s_full[0], t);
+          if (f & kKvUse1) mma_S(bQ1, tS1, bars->s_full[1], t);
+          mma_commit(smem_u32(&bars->k_empty[t % C::kKStages]));
+          if (f & kKvItemLast) mma_commit(smem_u32(&bars->q_empty));
+          for (;; ++t) {
+            const bool next = !(f & kKvItemLast);
+            if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
+            int fn = 0;  // flags of the next kv tile
+            if (next) {
+              if (!(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
+                break;
+              fn = flag(bars->kv_flags[(t + 1) % C::kKStages]);
+            }
+            if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
+                            f & kKvUse0, f & kKvFirst0, f & kKvLast0, fn & kKvUse0, t)))
+              break;
+            if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
+                            f & kKvUse1, f & kKvFirst1, f & kKvLast1, fn & kKvUse1, t)))
+              break;
+            mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
+            if (!next) break;
+            mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
+            if (fn & kKvItemLast) mma_commit(smem_u32(&bars->q_empty));  // after the last S
+            f = fn;
+          }
+          if (!ok) break;
+          kv_it = t + 1;
+        } else {
+          const int n = hi1 - lo0 + 1;  // kv tiles loaded for the item, from lo0
+          // S of the first kv tile (tile 1 joins later when its band starts later)
+          if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
+          mma_S(bQ0, tS0, bars->s_full[0], kv_it);
+          if (lo1 == lo0) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
+          mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
+          if (n == 1) mma_commit(smem_u32(&bars->q_empty));
+          for (int r = 0; ok && r < n; ++r) {
+            const int j = lo0 + r;
+            const uint32_t t = kv_it + r;
+            const bool next = r + 1 < n;
+            if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
+            if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
+              break;
+            // tile 0's range starts at lo0 and tile 1's ends at hi1 = lo0 + n - 1
+            if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
+                            j <= hi0, r == 0, j == hi0, j + 1 <= hi0, t)))
+              break;
+            if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
+                            j >= lo1, j == lo1, !next, next && j + 1 >= lo1, t)))
+              break;
+            mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
+            if (next) {
+              mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
+              if (r + 2 == n) mma_commit(smem_u32(&bars->q_empty));  // after the last S
+            }
+          }
+          if (!ok) break;
+          kv_it += n;
         }
-        if (!ok) break;
-        kv_it += n;
       }
       if (!ok) {
         mma_commit(smem_u32(&bars->drain));
@@ -383,8 +474,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int qidx = qt * kTile + r;
       float m = -INFINITY, l = 0.f;
       bool started = false;  // this Q tile has had a kv tile
-      for (int j = jlo; j <= jhi; ++j) {
-        if (kMask && !kv_used<kMask>(sh, it, w, j, jlo, jhi)) continue;
+      // kv tiles jlo .. jhi in order; with a block mask MaskOrder's subsequence
+      // for this Q tile (first the tiles both Q tiles keep, then its own),
+      // found 32 tiles at a time: each lane reads one mask byte, ballots
+      // gather them (sweep 0: both keep, sweep 1: only this one)
+      int sweep = 0, c0 = jlo - 32;
+      uint32_t bits = 0;
+      auto next_j = [&]() -> int {
+        while (bits == 0) {
+          c0 += 32;
+          if (c0 > jhi) {
+            if (sweep == 1) return INT_MAX;
+            sweep = 1;
+            c0 = jlo;
+          }
+          const int jj = c0 + lane;
+          const uint32_t mine = __ballot_sync(0xffffffffu, kv_used<kMask>(sh, it, w, jj, jlo, jhi));
+          const uint32_t other = __ballot_sync(
+              0xffffffffu, kv_used<kMask>(sh, it, w ^ 1, jj, w ? lo0 : lo1, w ? hi0 : hi1));
+          bits = sweep == 0 ? (mine & other) : (mine & ~other);
+        }
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        return c0 + b;
+      };
+      for (int j = kMask ? next_j() : jlo; j <= jhi; j = kMask ? next_j() : j + 1) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full[w]), cnt & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[4][32];
