@@ -36,7 +36,7 @@ EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status"
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
             "attn_profile_main_kernel", "attn_bwd_noalloc", "attn_step_host_scratch_size",
             "attn_step_host", "attn_step_host_status", "attn_fwd_window", "attn_bwd_window",
-            "attn_fwd_blocksparse", "attn_bwd_blocksparse")
+            "attn_fwd_ex", "attn_bwd_ex")
 BLOCK = 128  # rows per block of a block-sparse mask
 
 _lock = threading.Lock()
@@ -68,12 +68,12 @@ def load():
         lib.attn_bwd_window.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F,
                                         P, I, I, P, SZ, P]
         lib.attn_bwd_window.restype = I
-        lib.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, I, I, F,
-                                             P, I, P]
-        lib.attn_fwd_blocksparse.restype = I
-        lib.attn_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
-                                             P, I, I, F, P, I, I, P, SZ, P]
-        lib.attn_bwd_blocksparse.restype = I
+        lib.attn_fwd_ex.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, I, I, F, P, P,
+                                    I, P]
+        lib.attn_fwd_ex.restype = I
+        lib.attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, I, I,
+                                    F, P, P, I, I, P, SZ, P]
+        lib.attn_bwd_ex.restype = I
         lib.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_size.restype = SZ
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P,
@@ -165,28 +165,27 @@ def attn_bwd_window(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, 
                                   _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
-def attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left,
-                         window_right, block_mask, mask_batches, mask_heads, scale,
-                         cu_seqlens=None, layout=LAYOUT_BTHD, stream=None) -> int:
-    cu = _HostInts(cu_seqlens)
-    return load().attn_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq,
-                                       Tk, dqk, dv, int(causal), int(window_left),
-                                       int(window_right), _ptr(block_mask), int(mask_batches),
-                                       int(mask_heads), float(scale), cu.ptr, layout,
-                                       _stream(stream))
+def attn_fwd_ex(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left, window_right,
+                block_mask, mask_batches, mask_heads, scale, cu_seqlens_q=None,
+                cu_seqlens_k=None, layout=LAYOUT_BTHD, stream=None) -> int:
+    cq, ck = _HostInts(cu_seqlens_q), _HostInts(cu_seqlens_k)
+    return load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, dqk,
+                              dv, int(causal), int(window_left), int(window_right),
+                              _ptr(block_mask), int(mask_batches), int(mask_heads), float(scale),
+                              cq.ptr, ck.ptr, layout, _stream(stream))
 
 
-def attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
-                         window_left, window_right, block_mask, mask_batches, mask_heads, scale,
-                         cu_seqlens=None, layout=LAYOUT_BTHD, deterministic=False,
-                         workspace=None, workspace_bytes=0, stream=None) -> int:
-    cu = _HostInts(cu_seqlens)
-    return load().attn_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
-                                       _ptr(dq), _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv,
-                                       int(causal), int(window_left), int(window_right),
-                                       _ptr(block_mask), int(mask_batches), int(mask_heads),
-                                       float(scale), cu.ptr, layout, int(deterministic),
-                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
+def attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal, window_left,
+                window_right, block_mask, mask_batches, mask_heads, scale, cu_seqlens_q=None,
+                cu_seqlens_k=None, layout=LAYOUT_BTHD, deterministic=False, workspace=None,
+                workspace_bytes=0, stream=None) -> int:
+    cq, ck = _HostInts(cu_seqlens_q), _HostInts(cu_seqlens_k)
+    return load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv_out), B, H, Tq, Tk, dqk, dv, int(causal),
+                              int(window_left), int(window_right), _ptr(block_mask),
+                              int(mask_batches), int(mask_heads), float(scale), cq.ptr, ck.ptr,
+                              layout, int(deterministic), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream))
 
 
 def _mask_dims(block_mask):
@@ -310,11 +309,13 @@ def _dims(q, k, v, cu_seqlens, layout):
 
 
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BTHD,
-            with_lse=True, stream=None, window=None, block_mask=None):
+            with_lse=True, stream=None, window=None, block_mask=None, cu_seqlens_k=None):
     """O (bf16, like q with v's head size) and LSE (fp32) or None.
     window: (left, right) local-attention bounds (-1: open side), or None.
     block_mask: device uint8 [NQ][NK] or [Bm][Hm][NQ][NK] (NQ, NK: blocks of
-    BLOCK rows), non-zero = the block pair takes part, or None."""
+    BLOCK rows), non-zero = the block pair takes part, or None.
+    cu_seqlens_k: key offsets of a variable-length batch when they differ
+    from cu_seqlens (the query offsets), or None."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
     o = torch.empty(q.shape[:-2] + (H, dv), dtype=torch.bfloat16, device=q.device)
@@ -324,8 +325,8 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BT
                           dtype=torch.float32, device=q.device)
     wl, wr = (-1, -1) if window is None else window
     bm, mb, mh = _mask_dims(block_mask)
-    rc = attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, wl, wr, bm, mb, mh,
-                              scale, cu_seqlens, layout, stream)
+    rc = attn_fwd_ex(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, wl, wr, bm, mb, mh, scale,
+                     cu_seqlens, cu_seqlens_k, layout, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return o, lse
@@ -333,9 +334,9 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, layout=LAYOUT_BT
 
 def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
              layout=LAYOUT_BTHD, deterministic=False, workspace=None, stream=None, out=None,
-             window=None, block_mask=None):
+             window=None, block_mask=None, cu_seqlens_k=None):
     """(dq, dk, dv) as bf16 tensors shaped like q, k, v (a packed buffer for layout 1).
-    window, block_mask: as in forward()."""
+    window, block_mask, cu_seqlens_k: as in forward()."""
     B, H, Tq, Tk, dqk, dv = _dims(q, k, v, cu_seqlens, layout)
     scale = 1.0 / math.sqrt(dqk) if scale is None else scale
     if out is not None:
@@ -352,9 +353,9 @@ def backward(q, k, v, o, dO, lse, causal=False, scale=None, cu_seqlens=None,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wl, wr = (-1, -1) if window is None else window
     bm, mb, mh = _mask_dims(block_mask)
-    rc = attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, wl,
-                              wr, bm, mb, mh, scale, cu_seqlens, layout, deterministic, workspace,
-                              workspace.numel() * workspace.element_size(), stream)
+    rc = attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dvt, B, H, Tq, Tk, dqk, dv, causal, wl, wr, bm,
+                     mb, mh, scale, cu_seqlens, cu_seqlens_k, layout, deterministic, workspace,
+                     workspace.numel() * workspace.element_size(), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dvt

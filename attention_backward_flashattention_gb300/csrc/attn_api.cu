@@ -41,20 +41,29 @@ int num_sms_current() {
   return cache[dev];
 }
 
-// Common shape checks of attn_fwd / attn_bwd.  Returns ATTN_OK or an error.
+// Common shape checks of the forward and backward entry points.  cu / cuk:
+// query / key offsets of a variable-length batch (cuk == cu when the keys
+// share the queries' offsets).  Returns ATTN_OK or an error.
 int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const int* cu,
-                int layout, int wl = -1, int wr = -1) {
+                const int* cuk, int layout, int wl = -1, int wr = -1) {
   if (wl < -1 || wr < -1) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || Tq <= 0 || Tk <= 0) return ATTN_ERR_INVALID_ARG;
   if (layout != ATTN_LAYOUT_BTHD && layout != ATTN_LAYOUT_PACKED_QKV) return ATTN_ERR_INVALID_ARG;
   if (!supported_dims(dqk, dv)) return ATTN_ERR_UNSUPPORTED;
-  if (layout == ATTN_LAYOUT_PACKED_QKV && (dqk != dv || Tq != Tk)) return ATTN_ERR_UNSUPPORTED;
+  if (layout == ATTN_LAYOUT_PACKED_QKV && (dqk != dv || Tq != Tk || cu != cuk))
+    return ATTN_ERR_UNSUPPORTED;
+  if (cu == nullptr && cuk != nullptr) return ATTN_ERR_INVALID_ARG;
   if (cu != nullptr) {
     if (B > ATTN_MAX_VARLEN_SEQS) return ATTN_ERR_UNSUPPORTED;
-    if (Tq != Tk) return ATTN_ERR_INVALID_ARG;
-    if (cu[0] != 0 || cu[B] != Tq) return ATTN_ERR_INVALID_ARG;
-    for (int b = 0; b < B; ++b)
-      if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[B] != Tq || cuk[0] != 0 || cuk[B] != Tk) return ATTN_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b) {
+      const int lq = cu[b + 1] - cu[b], lk = cuk[b + 1] - cuk[b];
+      if (lq < 0 || lk < 0) return ATTN_ERR_INVALID_ARG;
+      // queries need keys; a causal or windowed sequence needs Lq <= Lk
+      // (its queries are the last Lq key positions)
+      if (lq > 0 && lk == 0) return ATTN_ERR_INVALID_ARG;
+      if ((causal || wl >= 0 || wr >= 0) && lq > lk) return ATTN_ERR_UNSUPPORTED;
+    }
   } else {
     // causal (or a local window) with fewer queries than keys aligns the
     // queries with the last Tq keys; more queries than keys would leave rows
@@ -67,31 +76,39 @@ int check_shape(int B, int H, int Tq, int Tk, int dqk, int dv, int causal, const
   return ATTN_OK;
 }
 
-int order_impl(const int* cu, int nseq, int* order) {
-  if (cu == nullptr || order == nullptr || nseq <= 0 || nseq > ATTN_MAX_VARLEN_SEQS)
+// Sequences by work, Lq * Lk, most first (ties: lower index first); with
+// shared offsets (cuk == cu) that is longest first.
+int order_impl(const int* cu, const int* cuk, int nseq, int* order) {
+  if (cu == nullptr || cuk == nullptr || order == nullptr || nseq <= 0 ||
+      nseq > ATTN_MAX_VARLEN_SEQS)
     return ATTN_ERR_INVALID_ARG;
   for (int b = 0; b < nseq; ++b) {
-    if (cu[b + 1] < cu[b]) return ATTN_ERR_INVALID_ARG;
+    if (cu[b + 1] < cu[b] || cuk[b + 1] < cuk[b]) return ATTN_ERR_INVALID_ARG;
     order[b] = b;
   }
-  std::stable_sort(order, order + nseq, [cu](int a, int b) {
-    return (cu[a + 1] - cu[a]) > (cu[b + 1] - cu[b]);
-  });
+  auto work = [cu, cuk](int b) {
+    return (int64_t)(cu[b + 1] - cu[b]) * (int64_t)(cuk[b + 1] - cuk[b]);
+  };
+  std::stable_sort(order, order + nseq, [&](int a, int b) { return work(a) > work(b); });
   return ATTN_OK;
 }
 
-// Variable-length tables: sequences longest first; items per sequence are
-// (tiles of that sequence) x H; q-tiles numbered sequence by sequence.
-void build_tables(const int* cu, int nseq, int H, int unit_rows, VarlenTables* t, int* n_items,
-                  int* n_qtiles) {
+// Variable-length tables: sequences by work; items per sequence are (its
+// 256-row query units (forward) or kv-tiles (backward)) x H; q-tiles numbered
+// sequence by sequence.
+void build_tables(const int* cu, const int* cuk, int nseq, int H, bool forward, VarlenTables* t,
+                  int* n_items, int* n_qtiles) {
   std::memset(t, 0, sizeof(*t));
-  for (int b = 0; b <= nseq; ++b) t->cu[b] = cu[b];
-  order_impl(cu, nseq, t->order);
+  for (int b = 0; b <= nseq; ++b) {
+    t->cu[b] = cu[b];
+    t->cuk[b] = cuk[b];
+  }
+  order_impl(cu, cuk, nseq, t->order);
   int acc = 0;
   for (int k = 0; k < nseq; ++k) {
     t->item_start[k] = acc;
     const int s = t->order[k];
-    acc += cdiv(cu[s + 1] - cu[s], unit_rows) * H;
+    acc += (forward ? cdiv(cu[s + 1] - cu[s], kFwdRows) : cdiv(cuk[s + 1] - cuk[s], kTile)) * H;
   }
   t->item_start[nseq] = acc;
   *n_items = acc;
@@ -149,7 +166,7 @@ int cuda_err(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 // Block-mask fields of the kernels' shape (mask may be null).  Returns
 // ATTN_OK or ATTN_ERR_INVALID_ARG.
 int set_block_mask(SeqShape* sh, const unsigned char* mask, int mask_batches, int mask_heads,
-                   int B, int H, int Tq, int Tk, const int* cu) {
+                   int B, int H, int Tq, int Tk, const int* cu, const int* cuk) {
   sh->blk = nullptr;
   sh->blk_bstride = sh->blk_hstride = 0;
   sh->blk_nk = 0;
@@ -157,10 +174,14 @@ int set_block_mask(SeqShape* sh, const unsigned char* mask, int mask_batches, in
   if ((mask_batches != 1 && mask_batches != B) || (mask_heads != 1 && mask_heads != H))
     return ATTN_ERR_INVALID_ARG;
   int nq = cdiv(Tq, kTile), nk = cdiv(Tk, kTile);
-  if (cu != nullptr) {  // blocks of the longest sequence
-    int longest = 0;
-    for (int b = 0; b < B; ++b) longest = std::max(longest, cu[b + 1] - cu[b]);
-    nq = nk = cdiv(longest, kTile);
+  if (cu != nullptr) {  // blocks of the longest sequence (queries, keys)
+    int lq = 0, lk = 0;
+    for (int b = 0; b < B; ++b) {
+      lq = std::max(lq, cu[b + 1] - cu[b]);
+      lk = std::max(lk, cuk[b + 1] - cuk[b]);
+    }
+    nq = cdiv(lq, kTile);
+    nk = cdiv(lk, kTile);
   }
   sh->blk = mask;
   sh->blk_nk = nk;
@@ -197,7 +218,7 @@ const char* attn_strerror(int code) {
 }
 
 int attn_varlen_order(const int* cu_seqlens, int nseq, int* order_out) {
-  return order_impl(cu_seqlens, nseq, order_out);
+  return order_impl(cu_seqlens, cu_seqlens, nseq, order_out);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int dqk, int dv, int varlen,
@@ -219,23 +240,27 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
                     int H, int Tq, int Tk, int dqk, int dv, int causal, int window_left,
                     int window_right, float scale, const int* cu_seqlens, int layout,
                     void* stream) {
-  return attn_fwd_blocksparse(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left,
-                              window_right, nullptr, 1, 1, scale, cu_seqlens, layout, stream);
+  return attn_fwd_ex(q, k, v, o, lse, B, H, Tq, Tk, dqk, dv, causal, window_left, window_right,
+                     nullptr, 1, 1, scale, cu_seqlens, nullptr, layout, stream);
 }
 
-int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
-                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
-                         int window_left, int window_right, const unsigned char* block_mask,
-                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
-                         int layout, void* stream) {
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Tq, int Tk, int dqk, int dv, int causal, int window_left, int window_right,
+                const unsigned char* block_mask, int mask_batches, int mask_heads, float scale,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int layout, void* stream) {
+  const int* cu_seqlens = cu_seqlens_q;
+  const int* cuk = cu_seqlens_k != nullptr ? cu_seqlens_k : cu_seqlens_q;
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;  // running max assumes s > 0
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID_ARG;
-  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout, window_left,
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, cuk, layout, window_left,
                        window_right);
   if (rc) return rc;
+  if (block_mask != nullptr && ((mask_batches != 1 && mask_batches != B) ||
+                                (mask_heads != 1 && mask_heads != H)))
+    return ATTN_ERR_INVALID_ARG;
 
   FwdLaunch L;
   std::memset(&L, 0, sizeof(L));
@@ -261,11 +286,12 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
   L.sh.wl = window_left;
   L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = 0;
-  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens);
+  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens,
+                      cuk);
   if (rc) return rc;
   if (varlen) {
     int n_items = 0, n_qt = 0;
-    build_tables(cu_seqlens, B, H, kFwdRows, &tables, &n_items, &n_qt);
+    build_tables(cu_seqlens, cuk, B, H, true, &tables, &n_items, &n_qt);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
@@ -304,18 +330,19 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     int Tk, int dqk, int dv, int causal, int window_left, int window_right,
                     float scale, const int* cu_seqlens, int layout, int deterministic,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
-                              window_left, window_right, nullptr, 1, 1, scale, cu_seqlens, layout,
-                              deterministic, workspace, workspace_bytes, stream);
+  return attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv, causal,
+                     window_left, window_right, nullptr, 1, 1, scale, cu_seqlens, nullptr, layout,
+                     deterministic, workspace, workspace_bytes, stream);
 }
 
-int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
-                         const void* dO, const float* lse, void* dq, void* dk, void* dv_out,
-                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
-                         int window_left, int window_right, const unsigned char* block_mask,
-                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
-                         int layout, int deterministic, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
+                int dqk, int dv, int causal, int window_left, int window_right,
+                const unsigned char* block_mask, int mask_batches, int mask_heads, float scale,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int layout, int deterministic,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  const int* cu_seqlens = cu_seqlens_q;
+  const int* cuk = cu_seqlens_k != nullptr ? cu_seqlens_k : cu_seqlens_q;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv_out || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -323,9 +350,12 @@ int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv_out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_INVALID_ARG;
-  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, layout, window_left,
+  int rc = check_shape(B, H, Tq, Tk, dqk, dv, causal, cu_seqlens, cuk, layout, window_left,
                        window_right);
   if (rc) return rc;
+  if (block_mask != nullptr && ((mask_batches != 1 && mask_batches != B) ||
+                                (mask_heads != 1 && mask_heads != H)))
+    return ATTN_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens != nullptr;
   if (workspace_bytes < attn_bwd_workspace_size(B, H, Tq, Tk, dqk, dv, varlen, deterministic))
     return ATTN_ERR_WORKSPACE_TOO_SMALL;
@@ -353,12 +383,13 @@ int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void
   L.sh.wl = window_left;
   L.sh.wr = causal ? 0 : window_right;
   L.sh.descending = deterministic ? 1 : 0;
-  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens);
+  rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens,
+                      cuk);
   if (rc) return rc;
   int n_qtiles;
   if (varlen) {
     int n_items = 0;
-    build_tables(cu_seqlens, B, H, kTile, &tables, &n_items, &n_qtiles);
+    build_tables(cu_seqlens, cuk, B, H, false, &tables, &n_items, &n_qtiles);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;

@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int p = 0; p < C::kVPanels; ++p)
           tma_load_3d(sV + p * kPanelBytes, &tm_v, kvb, p * 64, it.head, krow);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+        const int i0 = first_qtile(sh, it, it.tile), i1 = last_qtile(sh, it, it.tile, nq) + 1;
         const uint8_t* col = mask_col<kMask>(sh, it);
         for (int i = next_qtile(sh, col, i0, i1), inext; i < i1; i = inext, ++q_it) {
           inext = next_qtile(sh, col, i + 1, i1);
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (item >= sh.n_items) break;
         const Item it = decode_item(sh, tb, item, false);
         const int nq = cdiv(it.Lq, kTile);
-        const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+        const int i0 = first_qtile(sh, it, it.tile), i1 = last_qtile(sh, it, it.tile, nq) + 1;
         // Without a block mask the q-tiles are i0 .. i1-1.  With one, the
         // producer's per-stage flag says whether a stage's q-tile is the
         // item's last (read right after the stage's q_full wait, one step
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (item >= sh.n_items) break;
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
-      const int i0 = first_qtile(sh, it.tile), i1 = last_qtile(sh, it.tile, nq) + 1;
+      const int i0 = first_qtile(sh, it, it.tile), i1 = last_qtile(sh, it, it.tile, nq) + 1;
       const int kidx0 = it.tile * kTile + r;  // this thread's key
       const bool key_ok = kidx0 < it.Lk;
       const uint8_t* col = mask_col<kMask>(sh, it);
@@ -676,8 +676,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // (band bounds; -1 = open): this group's visible query columns are
         // [qmin, qmax), none for a key past the sequence end
         const int qrel = kidx0 - kTile * i - grp * 64;  // kidx - (first query of the group)
-        const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - sh.band_off - sh.wr)) : 0);
-        const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - sh.band_off + sh.wl + 1)) : 64;
+        const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - it.band_off - sh.wr)) : 0);
+        const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - it.band_off + sh.wl + 1)) : 64;
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -779,9 +779,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const Item it = decode_item(sh, tb, item, false);
       const int nq = cdiv(it.Lq, kTile);
       const int nk = cdiv(it.Lk, kTile);
-      const int i1 = last_qtile(sh, it.tile, nq) + 1;
+      const int i1 = last_qtile(sh, it, it.tile, nq) + 1;
       const uint8_t* col = mask_col<kMask>(sh, it);
-      const int ifirst = next_qtile(sh, col, first_qtile(sh, it.tile), i1);
+      const int ifirst = next_qtile(sh, col, first_qtile(sh, it, it.tile), i1);
       for (int i = ifirst; i < i1; i = next_qtile(sh, col, i + 1, i1), ++gi) {
         // deterministic order: contributions to q-tile i are added in
         // descending kv-tile order.  The tile's word holds 1 + the kv tile
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // contributor just above it: the next kv tile up within q-tile i's
         // band (that the block mask keeps).
         auto wait_target = [&]() {
-          const int last = last_kvtile(sh, i, nk);
+          const int last = last_kvtile(sh, it, i, nk);
           int above = it.tile + 1;
           if constexpr (kMask)
             while (above <= last && !tile_on(sh, it, i, above)) ++above;

@@ -39,8 +39,9 @@ constexpr int kMaxSeqs = 1024;  // sequences in one variable-length call
 
 // Host-computed tables for variable-length batches (passed by value).
 struct VarlenTables {
-  int cu[kMaxSeqs + 1];          // token offset of each sequence
-  int order[kMaxSeqs];           // sequences, longest first (ties: lower id first)
+  int cu[kMaxSeqs + 1];          // token offset of each sequence's queries
+  int cuk[kMaxSeqs + 1];         // ... and of its keys (equal to cu unless given apart)
+  int order[kMaxSeqs];           // sequences, most work (Lq * Lk) first (ties: lower id first)
   int item_start[kMaxSeqs + 1];  // first work item of the k-th sequence in `order`
   int tile_start[kMaxSeqs + 1];  // first q-tile of sequence s in the workspace tile space
                                  // (item_start counts 256-row units in the forward)
@@ -51,16 +52,17 @@ struct SeqShape {
   int nseq;        // B (number of sequences)
   int H;           // heads
   int varlen;      // 1: lengths come from VarlenTables
-  int Tq, Tk;      // fixed-length sequence lengths (varlen: unused)
+  int Tq, Tk;      // fixed-length sequence lengths (varlen: total token counts)
   int nq_tiles;    // fixed-length: ceil(Tq/128)
   int nk_tiles;    // fixed-length: ceil(Tk/128)
   int nq_units;    // fixed-length: ceil(Tq/256), forward work items per (b, h)
   int n_items;     // number of work items of the kernel
   int causal;
   // The band of visible keys: key j is visible to query i iff
-  //   i + band_off - wl <= j <= i + band_off + wr   (wl, wr = -1: that side open)
-  // causal is wr = 0; band_off = Tk - Tq for fixed length (the queries are the
-  // last Tq positions of the key sequence), 0 for variable length.
+  //   i + off - wl <= j <= i + off + wr   (wl, wr = -1: that side open)
+  // causal is wr = 0; off = Lk - Lq of the sequence (the queries are the last
+  // Lq positions of the key sequence), kept per item (Item::band_off);
+  // band_off here is the fixed-length Tk - Tq.
   int band_off;
   int wl, wr;
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
@@ -75,8 +77,10 @@ struct SeqShape {
 
 struct Item {
   int seq, head, tile;  // tile = q-tile (forward) or kv-tile (backward)
-  int row0;             // first token row of the sequence
-  int Lq, Lk;           // sequence lengths
+  int row0;             // first token row of the sequence's queries
+  int krow0;            // first token row of its keys
+  int Lq, Lk;           // sequence lengths (queries, keys)
+  int band_off;         // Lk - Lq: query i sits at key position i + band_off
   int tile_base;        // first q-tile of this sequence in the workspace tile space
 };
 
@@ -108,7 +112,9 @@ __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const 
   it.head = bh - it.seq * sh.H;
   it.Lq = sh.Tq;
   it.Lk = sh.Tk;
-  it.row0 = it.seq * sh.Tq;  // query rows; the keys start at key_row0() (seq * Tk)
+  it.row0 = it.seq * sh.Tq;
+  it.krow0 = it.seq * sh.Tk;
+  it.band_off = sh.band_off;
   it.tile_base = it.seq * sh.nq_tiles;
   return it;
 }
@@ -127,8 +133,12 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   it.seq = tb.order[lo];
   const int local = item - tb.item_start[lo];
   it.row0 = tb.cu[it.seq];
-  it.Lq = it.Lk = tb.cu[it.seq + 1] - it.row0;
-  const int nt = cdiv(it.Lq, forward ? kFwdRows : kTile);
+  it.krow0 = tb.cuk[it.seq];
+  it.Lq = tb.cu[it.seq + 1] - it.row0;
+  it.Lk = tb.cuk[it.seq + 1] - it.krow0;
+  it.band_off = it.Lk - it.Lq;
+  // forward items: 256-row query units; backward items: kv-tiles
+  const int nt = forward ? cdiv(it.Lq, kFwdRows) : cdiv(it.Lk, kTile);
   int rank;
   if (forward) {  // tile rank, then head
     rank = local / sh.H;
@@ -148,19 +158,19 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
 // the band when any of its (query, key) pairs is).  Numerators of the clamped
 // bounds may be negative; C++ division truncates toward zero, which the clamp
 // to 0 (first_*) absorbs and last_qtile corrects.
-__device__ __forceinline__ int first_kvtile(const SeqShape& sh, int qt) {
-  return sh.wl >= 0 ? max(0, (qt * kTile + sh.band_off - sh.wl) / kTile) : 0;
+__device__ __forceinline__ int first_kvtile(const SeqShape& sh, const Item& it, int qt) {
+  return sh.wl >= 0 ? max(0, (qt * kTile + it.band_off - sh.wl) / kTile) : 0;
 }
-__device__ __forceinline__ int last_kvtile(const SeqShape& sh, int qt, int nk) {
-  return sh.wr >= 0 ? min(nk - 1, (qt * kTile + kTile - 1 + sh.band_off + sh.wr) / kTile)
+__device__ __forceinline__ int last_kvtile(const SeqShape& sh, const Item& it, int qt, int nk) {
+  return sh.wr >= 0 ? min(nk - 1, (qt * kTile + kTile - 1 + it.band_off + sh.wr) / kTile)
                     : nk - 1;
 }
-__device__ __forceinline__ int first_qtile(const SeqShape& sh, int kt) {
-  return sh.wr >= 0 ? max(0, (kt * kTile - sh.band_off - sh.wr) / kTile) : 0;
+__device__ __forceinline__ int first_qtile(const SeqShape& sh, const Item& it, int kt) {
+  return sh.wr >= 0 ? max(0, (kt * kTile - it.band_off - sh.wr) / kTile) : 0;
 }
-__device__ __forceinline__ int last_qtile(const SeqShape& sh, int kt, int nq) {
+__device__ __forceinline__ int last_qtile(const SeqShape& sh, const Item& it, int kt, int nq) {
   if (sh.wl < 0) return nq - 1;
-  const int num = kt * kTile + kTile - 1 - sh.band_off + sh.wl;
+  const int num = kt * kTile + kTile - 1 - it.band_off + sh.wl;
   return num < 0 ? -1 : min(nq - 1, num / kTile);
 }
 
@@ -172,9 +182,7 @@ __device__ __forceinline__ bool tile_on(const SeqShape& sh, const Item& it, int 
                (int64_t)qt * sh.blk_nk + kt) != 0;
 }
 
-// First token row of the keys of a sequence (fixed-length Tk may differ from Tq).
-__device__ __forceinline__ int key_row0(const SeqShape& sh, const Item& it) {
-  return sh.varlen ? it.row0 : it.seq * sh.Tk;
-}
+// First token row of the keys of a sequence.
+__device__ __forceinline__ int key_row0(const SeqShape&, const Item& it) { return it.krow0; }
 
 }  // namespace attn

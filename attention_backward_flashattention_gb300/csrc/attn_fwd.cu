@@ -128,10 +128,10 @@ constexpr int kKvUse0 = 1, kKvUse1 = 2, kKvFirst0 = 4, kKvLast0 = 8, kKvFirst1 =
 __device__ __forceinline__ void kv_ranges(const SeqShape& sh, const Item& it, int& lo0, int& hi0,
                                           int& lo1, int& hi1) {
   const int nk = cdiv(it.Lk, kTile);
-  hi0 = last_kvtile(sh, 2 * it.tile, nk);
-  lo0 = min(first_kvtile(sh, 2 * it.tile), hi0);
-  hi1 = last_kvtile(sh, 2 * it.tile + 1, nk);
-  lo1 = min(first_kvtile(sh, 2 * it.tile + 1), hi1);
+  hi0 = last_kvtile(sh, it, 2 * it.tile, nk);
+  lo0 = min(first_kvtile(sh, it, 2 * it.tile), hi0);
+  hi1 = last_kvtile(sh, it, 2 * it.tile + 1, nk);
+  lo1 = min(first_kvtile(sh, it, 2 * it.tile + 1), hi1);
 }
 
 // Whether Q tile w (0, 1) of the item uses kv tile j: j lies in the tile's
@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // some row of the tile does not see all of its keys: the band's right
         // edge (first row) or left edge (last row) crosses it, or it is ragged
         const bool need_mask =
-            (sh.wr >= 0 && kbase + kTile - 1 > qt * kTile + sh.band_off + sh.wr) ||
-            (sh.wl >= 0 && kbase < qt * kTile + kTile - 1 + sh.band_off - sh.wl) ||
+            (sh.wr >= 0 && kbase + kTile - 1 > qt * kTile + it.band_off + sh.wr) ||
+            (sh.wl >= 0 && kbase < qt * kTile + kTile - 1 + it.band_off - sh.wl) ||
             (kbase + kTile > it.Lk);
         // row maximum over 8 independent chains (a single chain is latency-bound)
         float mx[8];
@@ -518,9 +518,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
         if (need_mask) {  // edge or ragged tile: keys outside the row's band -> -inf
           // this row's visible keys, relative to the tile: [klo, khi)
-          const int klo = sh.wl >= 0 ? qidx + sh.band_off - sh.wl - kbase : INT_MIN / 2;
+          const int klo = sh.wl >= 0 ? qidx + it.band_off - sh.wl - kbase : INT_MIN / 2;
           const int khi =
-              min(it.Lk, sh.wr >= 0 ? qidx + sh.band_off + sh.wr + 1 : it.Lk) - kbase;
+              min(it.Lk, sh.wr >= 0 ? qidx + it.band_off + sh.wr + 1 : it.Lk) - kbase;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll

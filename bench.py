@@ -442,14 +442,14 @@ def run_block_sparse(args, rank, world):
     wl, wr = -1, -1
 
     def fwd():
-        rc = binding.attn_fwd_blocksparse(q, k, v, o, lse, B, H, T, T, dqk, dv, w.causal, wl, wr,
-                                          bm, 1, H, w.scale, None, 0, stream)
+        rc = binding.attn_fwd_ex(q, k, v, o, lse, B, H, T, T, dqk, dv, w.causal, wl, wr, bm, 1,
+                                 H, w.scale, None, None, 0, stream)
         assert rc == 0, rc
 
     def bwd():
-        rc = binding.attn_bwd_blocksparse(q, k, v, o, dO, lse, dq, dk, dvt, B, H, T, T, dqk, dv,
-                                          w.causal, wl, wr, bm, 1, H, w.scale, None, 0, False, ws,
-                                          need, stream)
+        rc = binding.attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dvt, B, H, T, T, dqk, dv, w.causal,
+                                 wl, wr, bm, 1, H, w.scale, None, None, 0, False, ws, need,
+                                 stream)
         assert rc == 0, rc
 
     for _ in range(args.warmup):

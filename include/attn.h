@@ -147,41 +147,59 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Block-sparse attention: as attn_fwd_window, and in addition key j is visible
- * to query i only where the block mask marks the pair of blocks
- * (i / ATTN_BLOCK, j / ATTN_BLOCK) with a non-zero byte.  The block-sparse
- * mask module of "深度学习反向传播优化：2-CTA MMA模式与内存访问优化" §5.1-5.2
- * (FlexAttention and block-sparse variants built from the same kernels by a
- * mask module alone): the kernels skip every tile pair the mask drops.
+ * The general forward: every option of the calls above in one entry point.
+ *
+ * Local window: as attn_fwd_window (window_left / window_right, -1 = open).
+ *
+ * Block-sparse attention: key j is visible to query i only where the block
+ * mask marks the pair of blocks (i / ATTN_BLOCK, j / ATTN_BLOCK) with a
+ * non-zero byte.  The block-sparse mask module of "深度学习反向传播优化：2-CTA
+ * MMA模式与内存访问优化" §5.1-5.2 (FlexAttention and block-sparse variants built
+ * from the same kernels by a mask module alone): the kernels skip every tile
+ * pair the mask drops.
  *   block_mask: DEVICE pointer to uint8 [mask_batches][mask_heads][NQ][NK],
  *     C order, read only, owned by the caller, unchanged until the call's work
  *     on `stream` is done.  NQ = ceil(Tq / ATTN_BLOCK), NK = ceil(Tk /
- *     ATTN_BLOCK); for variable-length batches NQ = NK = ceil(longest sequence
- *     / ATTN_BLOCK), and sequence b uses its own block coordinates (entries
- *     past its end are not read).  mask_batches is 1 (one mask for every
- *     sequence) or B; mask_heads is 1 or H.  NULL: attn_fwd_window.
- * A query row that sees no key gets O = 0 and LSE = -inf (and, in
- * attn_bwd_blocksparse, dQ = 0; it adds nothing to dK or dV).  Returns
- * ATTN_ERR_INVALID_ARG for other mask_batches / mask_heads values.
+ *     ATTN_BLOCK); for variable-length batches NQ = ceil(longest query
+ *     sequence / ATTN_BLOCK), NK likewise for the keys, and sequence b uses its
+ *     own block coordinates (entries past its ends are not read).
+ *     mask_batches is 1 (one mask for every sequence) or B; mask_heads is 1 or
+ *     H.  NULL: no block mask.
+ * A query row that sees no key gets O = 0 and LSE = -inf (and, in attn_bwd_ex,
+ * dQ = 0; it adds nothing to dK or dV).
+ *
+ * Variable-length batches with separate query and key lengths ("ops(8)..."
+ * §1.3: seq_len_q and seq_len_kv given apart): cu_seqlens_q (host, B + 1
+ * offsets into the (sum Tq, H, d) queries) and cu_seqlens_k (host, B + 1
+ * offsets into the (sum Tk, H, d) keys and values); Tq and Tk are the totals.
+ * cu_seqlens_k = NULL: the keys use cu_seqlens_q (Tq == Tk); both NULL: fixed
+ * length.  Within sequence b the queries are the last Lq = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] of its Lk key positions (causal and windows align
+ * bottom-right, as for fixed length); a causal or windowed sequence needs
+ * Lq <= Lk (ATTN_ERR_UNSUPPORTED otherwise), and a sequence with queries needs
+ * keys (ATTN_ERR_INVALID_ARG).  LSE is (H, sum Tq).  Packed QKV needs shared
+ * offsets.
+ *
+ * Returns ATTN_ERR_INVALID_ARG for other mask_batches / mask_heads values or
+ * offsets that do not start at 0, decrease, or do not end at the totals.
  */
-int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
-                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
-                         int window_left, int window_right, const unsigned char* block_mask,
-                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
-                         int layout, void* stream);
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Tq, int Tk, int dqk, int dv, int causal, int window_left, int window_right,
+                const unsigned char* block_mask, int mask_batches, int mask_heads, float scale,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int layout, void* stream);
 
 /*
- * Backward of attn_fwd_blocksparse (same mask arguments; lse from that
- * forward).  Workspace as for attn_bwd.  Deterministic mode adds the dQ
- * contributions of the kept key tiles in descending key-tile order.
+ * Backward of attn_fwd_ex (same options; lse from that forward).  Workspace as
+ * for attn_bwd (its size query takes Tq = the total query count and varlen =
+ * 1).  Deterministic mode adds the dQ contributions of the kept key tiles in
+ * descending key-tile order.
  */
-int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
-                         const void* dO, const float* lse, void* dq, void* dk, void* dv_out,
-                         int B, int H, int Tq, int Tk, int dqk, int dv, int causal,
-                         int window_left, int window_right, const unsigned char* block_mask,
-                         int mask_batches, int mask_heads, float scale, const int* cu_seqlens,
-                         int layout, int deterministic, void* workspace,
-                         size_t workspace_bytes, void* stream);
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq, int Tk,
+                int dqk, int dv, int causal, int window_left, int window_right,
+                const unsigned char* block_mask, int mask_batches, int mask_heads, float scale,
+                const int* cu_seqlens_q, const int* cu_seqlens_k, int layout, int deterministic,
+                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward for callers that cannot allocate device memory (a plugin whose host

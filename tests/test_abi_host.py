@@ -173,3 +173,39 @@ def test_window_rejects(lib):
                  workspace_bytes=1 << 30, stream=0)
     assert binding.attn_bwd_window(**bargs) == binding.ATTN_ERR_UNSUPPORTED
 
+
+
+def _ex_fwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=2, H=2, Tq=300, Tk=700, dqk=64, dv=64, causal=1,
+                window_left=-1, window_right=-1, block_mask=None, mask_batches=1, mask_heads=1,
+                scale=0.125, cu_seqlens_q=[0, 100, 300], cu_seqlens_k=[0, 200, 700], layout=0,
+                stream=0)
+    args.update(kw)
+    return binding.attn_fwd_ex(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_seqlens_k=[0, 200, 699]), "INVALID_ARG"),        # does not end at Tk
+    (dict(cu_seqlens_k=[1, 200, 700]), "INVALID_ARG"),        # does not start at 0
+    (dict(cu_seqlens_k=[0, 300, 200]), "INVALID_ARG"),        # decreasing
+    (dict(cu_seqlens_k=[0, 0, 700]), "INVALID_ARG"),          # queries without keys
+    (dict(cu_seqlens_k=[0, 50, 700]), "UNSUPPORTED"),         # causal, Lq 100 > Lk 50
+    (dict(causal=0, window_left=8, cu_seqlens_k=[0, 50, 700]), "UNSUPPORTED"),  # window too
+    (dict(cu_seqlens_q=None), "INVALID_ARG"),                 # key offsets without query ones
+    (dict(layout=1, Tq=700, cu_seqlens_q=[0, 200, 700],
+          cu_seqlens_k=[0, 250, 700]), "UNSUPPORTED"),        # packed needs shared offsets
+    (dict(block_mask=A, mask_batches=3), "INVALID_ARG"),      # neither 1 nor B
+])
+def test_ex_rejects(lib, kw, code):
+    assert _ex_fwd(**kw) == getattr(binding, "ATTN_ERR_" + code)
+
+
+def test_ex_backward_rejects_like_forward(lib):
+    args = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, dq=A, dk=A, dv_out=A, B=2, H=2, Tq=300, Tk=700,
+                dqk=64, dv=64, causal=1, window_left=-1, window_right=-1, block_mask=None,
+                mask_batches=1, mask_heads=1, scale=0.125, cu_seqlens_q=[0, 100, 300],
+                cu_seqlens_k=[0, 50, 700], layout=0, deterministic=0, workspace=A,
+                workspace_bytes=1 << 30, stream=0)
+    assert binding.attn_bwd_ex(**args) == binding.ATTN_ERR_UNSUPPORTED
+    args["cu_seqlens_k"] = [0, 0, 700]
+    assert binding.attn_bwd_ex(**args) == binding.ATTN_ERR_INVALID_ARG

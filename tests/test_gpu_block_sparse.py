@@ -170,6 +170,6 @@ def test_block_mask_argument_checks():
     lse = torch.empty(1, 2, 256, dtype=torch.float32, device=dev)
     bm = torch.ones(2, 2, dtype=torch.uint8, device=dev)
     for mb, mh in ((3, 1), (1, 3), (0, 1)):  # neither 1 nor B / H
-        rc = binding.attn_fwd_blocksparse(q, q, q, o, lse, 1, 2, 256, 256, 64, 64, 0, -1, -1, bm,
-                                          mb, mh, 0.125)
+        rc = binding.attn_fwd_ex(q, q, q, o, lse, 1, 2, 256, 256, 64, 64, 0, -1, -1, bm, mb, mh,
+                                 0.125)
         assert rc == binding.ATTN_ERR_INVALID_ARG, (mb, mh)
