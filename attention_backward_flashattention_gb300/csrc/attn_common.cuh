@@ -26,7 +26,7 @@
 //             first); deterministic mode runs n descending, which is also the
 //             order in which each dQ tile receives its contributions, so a CTA
 //             only ever waits on work that was claimed before its own.
-//   Variable-length batches run sequence by sequence, longest first.
+//   Variable-length batches run sequence by sequence, most work (Lq * Lk) first.
 #pragma once
 
 #include <stdint.h>
