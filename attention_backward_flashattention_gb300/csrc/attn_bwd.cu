@@ -676,8 +676,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // (band bounds; -1 = open): this group's visible query columns are
         // [qmin, qmax), none for a key past the sequence end
         const int qrel = kidx0 - kTile * i - grp * 64;  // kidx - (first query of the group)
-        const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - it.band_off - sh.wr)) : 0);
-        const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - it.band_off + sh.wl + 1)) : 64;
+        const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - band_off(sh, it) - sh.wr)) : 0);
+        const int qmax = sh.wl >= 0 ? min(64, max(0, qrel - band_off(sh, it) + sh.wl + 1)) : 64;
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {

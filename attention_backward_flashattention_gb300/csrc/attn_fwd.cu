@@ -282,6 +282,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int who = 3, k0 = 0, k1 = 0, r = 0;
         for (int j = kMask ? mask_order_next(ord, sh, it, lo0, hi0, lo1, hi1, who) : lo0; j <= hi1;
              j = kMask ? mask_order_next(ord, sh, it, lo0, hi0, lo1, hi1, who) : j + 1) {
+          // (never true without a mask — the band ranges leave no gap — but
+          // the kernel without one issues its loads measurably faster with it)
+          if (!kMask && !kv_used<kMask>(sh, it, 0, j, lo0, hi0) &&
+              !kv_used<kMask>(sh, it, 1, j, lo1, hi1))
+            continue;
           const uint32_t sk = kv_it % C::kKStages, sv = kv_it % C::kVStages;
           if (!(ok = mbar_wait(smem_u32(&bars->k_empty[sk]), ((kv_it / C::kKStages) & 1) ^ 1, ab)))
             break;
@@ -418,32 +423,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok) break;
           kv_it = t + 1;
         } else {
-          const int n = hi1 - lo0 + 1;  // kv tiles loaded for the item, from lo0
+          // without a block mask the kv tiles are lo0 .. hi1 (the two band
+          // ranges leave no gap); Q tile w uses those in [lo_w, hi_w].  (This
+          // form of the loop, a kv-tile cursor beside the step count and
+          // range tests for the flags, issues faster than one that derives
+          // the flags from the step count.)
+          auto u0 = [&](int jj) { return jj >= lo0 && jj <= hi0; };
+          auto u1 = [&](int jj) { return jj >= lo1 && jj <= hi1; };
+          const int n = hi1 - lo0 + 1;
+          int j = lo0;
           // S of the first kv tile (tile 1 joins later when its band starts later)
           if (!(ok = W(bars->k_full[kv_it % C::kKStages], (kv_it / C::kKStages) & 1))) break;
-          mma_S(bQ0, tS0, bars->s_full[0], kv_it);
-          if (lo1 == lo0) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
+          if (u0(j)) mma_S(bQ0, tS0, bars->s_full[0], kv_it);
+          if (u1(j)) mma_S(bQ1, tS1, bars->s_full[1], kv_it);
           mma_commit(smem_u32(&bars->k_empty[kv_it % C::kKStages]));
           if (n == 1) mma_commit(smem_u32(&bars->q_empty));
           for (int r = 0; ok && r < n; ++r) {
-            const int j = lo0 + r;
             const uint32_t t = kv_it + r;
             const bool next = r + 1 < n;
+            const int jn = next ? j + 1 : hi1 + 1;
             if (!(ok = W(bars->v_full[t % C::kVStages], (t / C::kVStages) & 1))) break;
             if (next && !(ok = W(bars->k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1)))
               break;
-            // tile 0's range starts at lo0 and tile 1's ends at hi1 = lo0 + n - 1
             if (!(ok = step(tS0, tO0, bQ0, bars->p_full[0], bars->s_full[0], bars->o_done[0], cnt0,
-                            j <= hi0, r == 0, j == hi0, j + 1 <= hi0, t)))
+                            u0(j), j == lo0, j == hi0, next && u0(jn), t)))
               break;
             if (!(ok = step(tS1, tO1, bQ1, bars->p_full[1], bars->s_full[1], bars->o_done[1], cnt1,
-                            j >= lo1, j == lo1, !next, next && j + 1 >= lo1, t)))
+                            u1(j), j == lo1, j == hi1, next && u1(jn), t)))
               break;
             mma_commit(smem_u32(&bars->v_empty[t % C::kVStages]));
             if (next) {
               mma_commit(smem_u32(&bars->k_empty[(t + 1) % C::kKStages]));
               if (r + 2 == n) mma_commit(smem_u32(&bars->q_empty));  // after the last S
             }
+            j = jn;
           }
           if (!ok) break;
           kv_it += n;
@@ -509,8 +522,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // some row of the tile does not see all of its keys: the band's right
         // edge (first row) or left edge (last row) crosses it, or it is ragged
         const bool need_mask =
-            (sh.wr >= 0 && kbase + kTile - 1 > qt * kTile + it.band_off + sh.wr) ||
-            (sh.wl >= 0 && kbase < qt * kTile + kTile - 1 + it.band_off - sh.wl) ||
+            (sh.wr >= 0 && kbase + kTile - 1 > qt * kTile + band_off(sh, it) + sh.wr) ||
+            (sh.wl >= 0 && kbase < qt * kTile + kTile - 1 + band_off(sh, it) - sh.wl) ||
             (kbase + kTile > it.Lk);
         // row maximum over 8 independent chains (a single chain is latency-bound)
         float mx[8];
@@ -518,9 +531,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
         if (need_mask) {  // edge or ragged tile: keys outside the row's band -> -inf
           // this row's visible keys, relative to the tile: [klo, khi)
-          const int klo = sh.wl >= 0 ? qidx + it.band_off - sh.wl - kbase : INT_MIN / 2;
+          const int klo = sh.wl >= 0 ? qidx + band_off(sh, it) - sh.wl - kbase : INT_MIN / 2;
           const int khi =
-              min(it.Lk, sh.wr >= 0 ? qidx + it.band_off + sh.wr + 1 : it.Lk) - kbase;
+              min(it.Lk, sh.wr >= 0 ? qidx + band_off(sh, it) + sh.wr + 1 : it.Lk) - kbase;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
