@@ -18,15 +18,17 @@
  * Tq == Tk that is the §2.2 CPU loop's t2 <= t; with fewer queries than keys
  * (separate query and key lengths, as the cuDNN graph of "ops(8)..." §1.3
  * allows) the queries are the last Tq positions of the key sequence
- * (bottom-right alignment).  Causal with Tq > Tk, and causal variable-length
- * batches with different query and key offsets, are not supported.
+ * (bottom-right alignment).  Causal (or windowed) attention with more queries
+ * than keys is not supported: Tq > Tk at fixed length, or a sequence with
+ * Lq > Lk in a variable-length batch with separate offsets (attn_fwd_ex).
  *
  * Precision.  Inputs and outputs are bf16; products accumulate in fp32; the
  * softmax runs in fp32; P and dS are rounded to bf16 before they enter the
  * tensor-core products; dQ is accumulated across key tiles in fp32.
  *
- * Memory.  Every pointer is a DEVICE pointer except `cu_seqlens` (host) and
- * the tensors of attn_step_host (host).
+ * Memory.  Every pointer is a DEVICE pointer except the offset tables
+ * `cu_seqlens`, `cu_seqlens_q`, `cu_seqlens_k` (host) and the tensors of
+ * attn_step_host (host).
  * The library allocates no device memory: the caller owns all buffers,
  * including the backward workspace, sized with attn_bwd_workspace_size().
  * Every tensor pointer must be 16-byte aligned.
@@ -44,7 +46,9 @@
  *       (Tq, H, d) (or (Tq, 3, H, d) packed), sequence b occupies rows
  *       cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32, host memory, B+1 entries,
  *       cu_seqlens[0] == 0, nondecreasing, cu_seqlens[B] == Tq), and LSE is
- *       (H, Tq).  At most ATTN_MAX_VARLEN_SEQS sequences.
+ *       (H, Tq).  At most ATTN_MAX_VARLEN_SEQS sequences.  attn_fwd_ex /
+ *       attn_bwd_ex also take separate key offsets (keys (Tk, H, d), Tk the
+ *       total key count).
  *   Fixed length: LSE is (B, H, Tq) fp32.
  *
  * Supported head sizes: (dqk, dv) in {(64, 64), (128, 128), (192, 128)}.
