@@ -18,12 +18,16 @@ BL = binding.BLOCK
 DIMS = [(64, 64), (128, 128), (192, 128)]
 
 
-def mixed_cases(n=12, seed=2024):
+def mixed_cases(n=16, seed=2024):
     rng = np.random.default_rng(seed)
     cases = []
     for c in range(n):
         d, dv = DIMS[c % 3]
         form = ["fixed", "varlen", "varlen_qk"][(c // 3) % 3]
+        packed = c >= 12  # the last cases use the packed (.., 3, H, d) layout
+        if packed:
+            d = dv = (64, 128)[c % 2]
+            form = ("fixed", "varlen")[(c // 2) % 2]
         causal = bool(rng.integers(2))
         window = None
         if rng.random() < 0.4:
@@ -36,6 +40,8 @@ def mixed_cases(n=12, seed=2024):
             B = int(rng.integers(1, 3))
             Tk = int(rng.integers(1, 700))
             Tq = int(rng.integers(1, Tk + 1)) if banded else int(rng.integers(1, 700))
+            if packed:
+                Tq = Tk
             lq, lk = (Tq,) * B, (Tk,) * B
         else:
             B = int(rng.integers(1, 5))
@@ -48,7 +54,7 @@ def mixed_cases(n=12, seed=2024):
         density = [None, 0.35, 0.75][int(rng.integers(3))]
         det = bool(rng.integers(2))
         cases.append(dict(id=c, d=d, dv=dv, form=form, causal=causal, window=window, H=H,
-                          lq=lq, lk=lk, density=density, det=det))
+                          lq=lq, lk=lk, density=density, det=det, packed=packed))
     return cases
 
 
@@ -84,6 +90,10 @@ def test_mixed_case_against_oracle(case):
     else:
         t = {n: x[n].to(dev) for n in x}
         kw = dict(cu_seqlens=cq, cu_seqlens_k=ck if case["form"] == "varlen_qk" else None)
+    if case["packed"]:  # q, k, v as slots of one (.., 3, H, d) buffer
+        qkv = torch.stack([t["q"], t["k"], t["v"]], dim=-3).contiguous()
+        t.update(q=qkv.select(-3, 0), k=qkv.select(-3, 1), v=qkv.select(-3, 2))
+        kw["layout"] = binding.LAYOUT_PACKED_QKV
     mask = bm = None
     nq, nk = -(-max(max(lq), 1) // BL), -(-max(lk) // BL)
     if case["density"] is not None:
