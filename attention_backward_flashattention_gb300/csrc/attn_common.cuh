@@ -155,7 +155,7 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
 
 // The band offset of the item's sequence, Lk - Lq.  Fixed-length items carry
 // the kernel-wide Tk - Tq, so this folds to the kernel parameter there.
-__device__ __forceinline__ int band_off(const SeqShape& sh, const Item& it) {
+__host__ __device__ __forceinline__ int band_off(const SeqShape& sh, const Item& it) {
   return sh.varlen ? it.band_off : sh.band_off;
 }
 
@@ -164,17 +164,17 @@ __device__ __forceinline__ int band_off(const SeqShape& sh, const Item& it) {
 // the band when any of its (query, key) pairs is).  Numerators of the clamped
 // bounds may be negative; C++ division truncates toward zero, which the clamp
 // to 0 (first_*) absorbs and last_qtile corrects.
-__device__ __forceinline__ int first_kvtile(const SeqShape& sh, const Item& it, int qt) {
+__host__ __device__ __forceinline__ int first_kvtile(const SeqShape& sh, const Item& it, int qt) {
   return sh.wl >= 0 ? max(0, (qt * kTile + band_off(sh, it) - sh.wl) / kTile) : 0;
 }
-__device__ __forceinline__ int last_kvtile(const SeqShape& sh, const Item& it, int qt, int nk) {
+__host__ __device__ __forceinline__ int last_kvtile(const SeqShape& sh, const Item& it, int qt, int nk) {
   return sh.wr >= 0 ? min(nk - 1, (qt * kTile + kTile - 1 + band_off(sh, it) + sh.wr) / kTile)
                     : nk - 1;
 }
-__device__ __forceinline__ int first_qtile(const SeqShape& sh, const Item& it, int kt) {
+__host__ __device__ __forceinline__ int first_qtile(const SeqShape& sh, const Item& it, int kt) {
   return sh.wr >= 0 ? max(0, (kt * kTile - band_off(sh, it) - sh.wr) / kTile) : 0;
 }
-__device__ __forceinline__ int last_qtile(const SeqShape& sh, const Item& it, int kt, int nq) {
+__host__ __device__ __forceinline__ int last_qtile(const SeqShape& sh, const Item& it, int kt, int nq) {
   if (sh.wl < 0) return nq - 1;
   const int num = kt * kTile + kTile - 1 - band_off(sh, it) + sh.wl;
   return num < 0 ? -1 : min(nq - 1, num / kTile);
