@@ -20,7 +20,8 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    with open(os.path.join(ROOT, "include", "attn.h")) as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", src, flags=re.M)
 
