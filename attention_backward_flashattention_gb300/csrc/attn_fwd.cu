@@ -9,7 +9,7 @@
 // key/value tiles, with a running row maximum and row sum) and §4.2 (the
 // division by the row sum happens once, after the loop).
 //
-// One CTA (320 threads) per SM, persistent over work items; an item is two
+// One CTA (384 threads) per SM, persistent over work items; an item is two
 // consecutive 128-row Q tiles of one (sequence, head) (see attn_common.cuh for
 // the order):
 //   warps 0-3, 4-7  softmax warpgroup w owns Q tile w: thread r holds query
@@ -23,6 +23,9 @@
 // shared memory.  The two warpgroups alternate: while one computes its P, the
 // tensor core runs the other tile's MMAs.  The running maximum is only moved
 // (and O rescaled) when it grows by more than 2^8, so most tiles skip it.
+// The kernels built for a block mask (kMask) visit only the kv tiles the mask
+// keeps, in the order MaskOrder describes, with the producer publishing each
+// tile's step flags to the MMA issuer.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -35,8 +38,9 @@ namespace attn {
 namespace {
 
 // Softmax warpgroups 0 and 1; warpgroup 2 holds the TMA warp (8) and the MMA
-// warp (9), warps 10-11 idle.  Launched with 384 x 168 registers; warpgroup 2
-// gives back (168 - 56) x 128, which the two softmax warpgroups take.
+// warp (9), warps 10-11 idle.  Launched with 168 registers a thread; warpgroup 2
+// drops to 128, which lets the two softmax warpgroups rise to 184
+// (2 x 184 + 128 <= 3 x 168).
 constexpr int kFwdThreads = 384;
 constexpr uint32_t kRegsCtl = 128;
 constexpr uint32_t kRegsSoftmax = 184;
