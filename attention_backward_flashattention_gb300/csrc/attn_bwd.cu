@@ -42,6 +42,10 @@
 // (second half), dP_{i+1}, dV_{i+1} ... so that P_{i+1} is computed while dK_i
 // and dQ_i run (S and dP have their own TMEM columns for d <= 128), and the
 // dQ drain overlaps the second half of dK_i.
+// The q-tiles of an item are those of its band (causal, window); the kernels
+// built for a block mask (kMask) walk only the ones the mask keeps.  In
+// deterministic mode each dQ tile's contributions arrive in descending kv-tile
+// order: a per-(q-tile, head) word holds 1 + the kv tile that added last.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
