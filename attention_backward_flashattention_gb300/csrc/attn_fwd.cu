@@ -191,17 +191,21 @@ __device__ __forceinline__ int mask_order_next(MaskOrder& o, const SeqShape& sh,
 }
 
 // kMask: built with block-mask support (sh.blk non-null); the kernels without
-// it carry none of the mask's walks.
-template <int DQK, int DV, typename Tables, bool kMask>
+// it carry none of the mask's walks.  kLeft: the band has a left edge (a
+// window's left bound, sh.wl >= 0); without one the kernel sees wl = -1 as a
+// constant and its left-edge tests fold away.
+template <int DQK, int DV, typename Tables, bool kMask, bool kLeft>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, const int64_t o_row_stride,
                     const int64_t lse_head_stride, const int64_t lse_seq_stride,
-                    const float scale_log2, int* status, const SeqShape sh,
+                    const float scale_log2, int* status, const SeqShape sh_in,
                     const __grid_constant__ Tables tb) {
   using C = FwdCfg<DQK, DV>;
+  SeqShape sh = sh_in;
+  if constexpr (!kLeft) sh.wl = -1;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled panels need a 1024-byte aligned window
     if (threadIdx.x == 0) atomicCAS(status, 0, kStatusInternal);
@@ -650,8 +654,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int DQK, int DV>
-cudaError_t launch_typed(const FwdLaunch& L) {
+template <int DQK, int DV, bool kMask, bool kLeft>
+cudaError_t launch_kernel(const FwdLaunch& L) {
   using C = FwdCfg<DQK, DV>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
@@ -659,8 +663,7 @@ cudaError_t launch_typed(const FwdLaunch& L) {
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = L.stream;
   if (L.tables) {
-    auto* k = L.sh.blk != nullptr ? attn_fwd_kernel<DQK, DV, VarlenTables, true>
-                                  : attn_fwd_kernel<DQK, DV, VarlenTables, false>;
+    auto* k = attn_fwd_kernel<DQK, DV, VarlenTables, kMask, kLeft>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v,
@@ -668,13 +671,19 @@ cudaError_t launch_typed(const FwdLaunch& L) {
                               L.lse_head_stride, L.lse_seq_stride, L.scale_log2, L.status, L.sh,
                               *L.tables);
   }
-  auto* k = L.sh.blk != nullptr ? attn_fwd_kernel<DQK, DV, NoTables, true>
-                                : attn_fwd_kernel<DQK, DV, NoTables, false>;
+  auto* k = attn_fwd_kernel<DQK, DV, NoTables, kMask, kLeft>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, reinterpret_cast<__nv_bfloat16*>(L.o),
                             L.lse, L.o_row_stride, L.lse_head_stride, L.lse_seq_stride,
                             L.scale_log2, L.status, L.sh, NoTables{});
+}
+
+template <int DQK, int DV>
+cudaError_t launch_typed(const FwdLaunch& L) {
+  const bool mask = L.sh.blk != nullptr, left = L.sh.wl >= 0;
+  if (mask) return left ? launch_kernel<DQK, DV, true, true>(L) : launch_kernel<DQK, DV, true, false>(L);
+  return left ? launch_kernel<DQK, DV, false, true>(L) : launch_kernel<DQK, DV, false, false>(L);
 }
 
 }  // namespace
