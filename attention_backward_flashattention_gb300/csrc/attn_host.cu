@@ -7,7 +7,7 @@
 // over the groups:
 //
 //   h2d stream:      copy q, k, v, dO of group g into device set g % 2
-//   compute stream:  attn_fwd + attn_bwd on set g % 2
+//   compute stream:  attn_fwd (once q, k, v are in) + attn_bwd (once dO is) on set g % 2
 //   d2h stream:      copy dq, dk, dv (and o) of set g % 2 into the host tensors
 //
 // so that group g+1's inputs travel and group g-1's gradients come back while
@@ -92,12 +92,13 @@ std::vector<int> group_sizes(int H, int G) {
 }
 
 struct Events {
-  cudaEvent_t entry = nullptr, h2d[2] = {}, comp[2] = {}, d2h[2] = {};
+  cudaEvent_t entry = nullptr, qkv[2] = {}, h2d[2] = {}, comp[2] = {}, d2h[2] = {};
   bool ok = true;
   Events() {
     ok = cudaEventCreateWithFlags(&entry, cudaEventDisableTiming) == cudaSuccess;
     for (int s = 0; s < 2 && ok; ++s)
-      ok = cudaEventCreateWithFlags(&h2d[s], cudaEventDisableTiming) == cudaSuccess &&
+      ok = cudaEventCreateWithFlags(&qkv[s], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h2d[s], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&comp[s], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&d2h[s], cudaEventDisableTiming) == cudaSuccess;
   }
@@ -106,6 +107,7 @@ struct Events {
   ~Events() {
     if (entry) cudaEventDestroy(entry);
     for (int s = 0; s < 2; ++s) {
+      if (qkv[s]) cudaEventDestroy(qkv[s]);
       if (h2d[s]) cudaEventDestroy(h2d[s]);
       if (comp[s]) cudaEventDestroy(comp[s]);
       if (d2h[s]) cudaEventDestroy(d2h[s]);
@@ -181,22 +183,25 @@ int attn_step_host(const void* q, const void* k, const void* v, const void* dO, 
     float* lse = reinterpret_cast<float*>(base + L.lse);
     void *gq = base + L.dq, *gk = base + L.dk, *gv = base + L.dv;
     void* ws = base + L.ws;
-    // stage 1: inputs (after the kernels of group g-2 are done with this set)
+    // stage 1: inputs (after the kernels of group g-2 are done with this set);
+    // q, k, v first: the forward needs only those, dO travels while it runs
     if (g >= 2 && cudaStreamWaitEvent(hs, ev.comp[s], 0) != cudaSuccess) return ATTN_ERR_CUDA;
     if (copy_slice(q_d, q, dqk, h0, Gg, H, rows, true, hs) ||
         copy_slice(k_d, k, dqk, h0, Gg, H, rows, true, hs) ||
         copy_slice(v_d, v, dv, h0, Gg, H, rows, true, hs) ||
+        cudaEventRecord(ev.qkv[s], hs) != cudaSuccess ||
         copy_slice(do_d, dO, dv, h0, Gg, H, rows, true, hs) ||
         cudaEventRecord(ev.h2d[s], hs) != cudaSuccess)
       return ATTN_ERR_CUDA;
     // stage 2: kernels (after the inputs, and after group g-2's results left)
     cudaStream_t c = css[s];
-    if (cudaStreamWaitEvent(c, ev.h2d[s], 0) != cudaSuccess ||
+    if (cudaStreamWaitEvent(c, ev.qkv[s], 0) != cudaSuccess ||
         (g >= 2 && cudaStreamWaitEvent(c, ev.d2h[s], 0) != cudaSuccess))
       return ATTN_ERR_CUDA;
     int rc = attn_fwd(q_d, k_d, v_d, o_d, lse, B, Gg, T, T, dqk, dv, causal, scale, nullptr,
                       ATTN_LAYOUT_BTHD, c);
     if (rc) return rc;
+    if (cudaStreamWaitEvent(c, ev.h2d[s], 0) != cudaSuccess) return ATTN_ERR_CUDA;
     rc = attn_bwd(q_d, k_d, v_d, o_d, do_d, lse, gq, gk, gv, B, Gg, T, T, dqk, dv, causal, scale,
                   nullptr, ATTN_LAYOUT_BTHD, deterministic, ws, L.ws_bytes, c);
     if (rc) return rc;
