@@ -210,3 +210,11 @@ def test_ex_backward_rejects_like_forward(lib):
     assert binding.attn_bwd_ex(**args) == binding.ATTN_ERR_UNSUPPORTED
     args["cu_seqlens_k"] = [0, 0, 700]
     assert binding.attn_bwd_ex(**args) == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No fallback: with the library absent the binding raises at first use."""
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libattn_gb300.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(Exception, match="missing"):
+        binding.load()
