@@ -64,6 +64,8 @@
  *   3: causal mask off by one (j < i)     4: dV indexed by the key's own row
  *   5: LSE returned in log base 2         6: dK takes dS^T K instead of dS^T Q
  *   7: block mask read transposed ([key block][query block])
+ *   8: window's left bound off by one (one key too many)
+ *   9: a row that sees no key returns LSE = 0 instead of -inf
  */
 #ifndef ORACLE_PLANT
 #define ORACLE_PLANT 0
@@ -82,7 +84,7 @@ static void visible_range(int causal, int wl, int wr, int i, int Tq, int Tk, int
   int l = 0, h = Tk - 1;
   if (causal) h = (ORACLE_PLANT == 3 && i > 0) ? i + off - 1 : i + off;
   if (wr >= 0 && i + off + wr < h) h = i + off + wr;
-  if (wl >= 0 && i + off - wl > l) l = i + off - wl;
+  if (wl >= 0 && i + off - wl - (ORACLE_PLANT == 8) > l) l = i + off - wl - (ORACLE_PLANT == 8);
   if (h > Tk - 1) h = Tk - 1;
   *lo = l;
   *hi = h;
@@ -149,7 +151,7 @@ static void forward_row(const double *q, const double *K, const double *V,
   if (o)
     for (int c = 0; c < dv; c++) o[c] = 0.0;
   if (n == 0) {
-    if (lse) *lse = -INFINITY;
+    if (lse) *lse = (ORACLE_PLANT == 9) ? 0.0 : -INFINITY;
     return;
   }
   double m = -INFINITY;

@@ -37,6 +37,17 @@ def _pins(oracle, lib):
     t = _torch_reference(q, k, v, dO, False, s, block_mask=bm, block=4)
     res["autograd_block_mask"] = all(
         rel_err(g[key], t[key]) <= 1e-10 for key in ("O", "dQ", "dK", "dV"))
+    # local window (Tq < Tk) against the autograd route
+    q, k, v, dO = _small(n=1, T=6, Tk=9, d=3, seed=6)
+    g = oracle.backward(q, k, v, dO, False, s, window=(2, 1), lib=lib)
+    t = _torch_reference(q, k, v, dO, False, s, window=(2, 1))
+    res["autograd_window"] = all(
+        rel_err(g[key], t[key]) <= 1e-10 for key in ("O", "dQ", "dK", "dV"))
+    # a query block that keeps no key block: LSE = -inf, O = 0
+    q, k, v, dO = _small(n=1, T=8, d=3, seed=8)
+    O, L, _ = oracle.forward(q, k, v, False, s, block_mask=[[1, 1], [0, 0]], block=4, lib=lib)
+    res["empty_rows"] = bool(np.all(np.isneginf(L[0, 4:])) and np.all(O[0, 4:] == 0)
+                             and np.all(np.isfinite(L[0, :4])))
     # last row: causal == non-causal
     q, k, v, dO = _small(n=1, T=6, d=3, seed=4)
     Oc, Lc, _ = oracle.forward(q, k, v, True, s, lib=lib)
@@ -60,7 +71,7 @@ def test_oracle_passes_every_pin(oracle_mod):
     assert all(res.values()), res
 
 
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_planted_mistake_is_caught(oracle_mod, plant):
     lib = oracle_mod.planted(plant)
     res = _pins(oracle_mod, lib)
