@@ -34,9 +34,10 @@ MAX_VARLEN_SEQS = 1024
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status",
             "attn_fwd_status", "attn_strerror", "attn_varlen_order", "attn_debug_set_wait_bias",
-            "attn_profile_main_kernel", "attn_bwd_noalloc", "attn_step_host_scratch_size",
-            "attn_step_host", "attn_step_host_status", "attn_fwd_window", "attn_bwd_window",
-            "attn_fwd_ex", "attn_bwd_ex")
+            "attn_profile_main_kernel", "attn_profile_aux_kernels", "attn_bwd_noalloc",
+            "attn_bwd_noalloc_status", "attn_step_host_scratch_size", "attn_step_host",
+            "attn_step_host_status", "attn_fwd_window", "attn_bwd_window", "attn_fwd_ex",
+            "attn_bwd_ex", "attn_debug_cache_stats")
 BLOCK = 128  # rows per block of a block-sparse mask
 
 _lock = threading.Lock()
@@ -82,6 +83,8 @@ def load():
         lib.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, I,
                                          I, P]
         lib.attn_bwd_noalloc.restype = I
+        lib.attn_bwd_noalloc_status.argtypes = [P]
+        lib.attn_bwd_noalloc_status.restype = I
         lib.attn_bwd_status.argtypes = [P, P]
         lib.attn_bwd_status.restype = I
         lib.attn_fwd_status.argtypes = [P]
@@ -92,6 +95,10 @@ def load():
         lib.attn_varlen_order.restype = I
         lib.attn_profile_main_kernel.argtypes = [P, P]
         lib.attn_profile_main_kernel.restype = I
+        lib.attn_profile_aux_kernels.argtypes = [P, P, P, P]
+        lib.attn_profile_aux_kernels.restype = I
+        lib.attn_debug_cache_stats.argtypes = [P]
+        lib.attn_debug_cache_stats.restype = I
         lib.attn_debug_set_wait_bias.argtypes = [I]
         lib.attn_debug_set_wait_bias.restype = I
         lib.attn_step_host_scratch_size.argtypes = [I, I, I, I, I, I, I]
@@ -228,6 +235,10 @@ def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv_out, B, H, Tq, Tk, dqk, dv,
                                    _stream(stream))
 
 
+def attn_bwd_noalloc_status(stream=None) -> int:
+    return load().attn_bwd_noalloc_status(_stream(stream))
+
+
 def attn_bwd_status(workspace, stream=None) -> int:
     return load().attn_bwd_status(_ptr(workspace), _stream(stream))
 
@@ -251,6 +262,24 @@ def attn_profile_main_kernel(event_start=None, event_stop=None) -> int:
     """Record torch.cuda.Event (or raw cudaEvent_t) pairs around the backward main kernel."""
     conv = lambda e: None if e is None else (e.cuda_event if hasattr(e, "cuda_event") else int(e))
     return load().attn_profile_main_kernel(conv(event_start), conv(event_stop))
+
+
+def attn_profile_aux_kernels(pre_start=None, pre_stop=None, convert_start=None,
+                             convert_stop=None) -> int:
+    """Record event pairs around the backward's preprocess and dQ conversion kernels."""
+    conv = lambda e: None if e is None else (e.cuda_event if hasattr(e, "cuda_event") else int(e))
+    return load().attn_profile_aux_kernels(conv(pre_start), conv(pre_stop), conv(convert_start),
+                                           conv(convert_stop))
+
+
+def attn_debug_cache_stats() -> dict:
+    """Host-side cache counters (tensor maps encoded / reused, tables built / reused)."""
+    out = (ctypes.c_longlong * 4)()
+    rc = load().attn_debug_cache_stats(ctypes.cast(out, ctypes.c_void_p))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_debug_cache_stats")
+    return {"map_encodes": out[0], "map_hits": out[1], "table_builds": out[2],
+            "table_hits": out[3]}
 
 
 def attn_debug_set_wait_bias(bias: int) -> int:

@@ -121,6 +121,103 @@ void build_tables(const int* cu, const int* cuk, int nseq, int H, bool forward, 
   *n_qtiles = tiles;
 }
 
+// Host-side cache of what every call would otherwise rebuild: the TMA tensor
+// maps (keyed by the base pointer and every encoding parameter) and the
+// variable-length schedule tables (keyed by the offsets' contents, the head
+// count and the kernel).  The cuDNN graph of "ops(8)..." §1.3 is built once
+// and executed many times; this is the same idea for the library's host work.
+// Least recently used entries are replaced; one mutex guards both caches.
+class HostCache {
+ public:
+  bool map(CUtensorMap* out, const void* base, int64_t d, int64_t heads, int64_t rows,
+           int64_t head_stride, int64_t row_stride, uint32_t box_rows) {
+    const MapKey key{base, d, heads, rows, head_stride, row_stride, box_rows};
+    std::lock_guard<std::mutex> g(mu_);
+    MapEntry* victim = &maps_[0];
+    for (MapEntry& e : maps_) {
+      if (e.used != 0 && std::memcmp(&e.key, &key, sizeof(key)) == 0) {
+        e.used = ++clock_;
+        *out = e.map;
+        ++stats_[1];
+        return true;
+      }
+      if (e.used < victim->used) victim = &e;
+    }
+    if (!make_panel_map(&victim->map, base, d, heads, rows, head_stride, row_stride, box_rows)) {
+      victim->used = 0;
+      return false;
+    }
+    victim->key = key;
+    victim->used = ++clock_;
+    *out = victim->map;
+    ++stats_[0];
+    return true;
+  }
+
+  void tables(const int* cu, const int* cuk, int nseq, int H, bool forward, VarlenTables* out,
+              int* n_items, int* n_qtiles) {
+    std::lock_guard<std::mutex> g(mu_);
+    TabEntry* victim = &tabs_[0];
+    for (TabEntry& e : tabs_) {
+      if (e.used != 0 && e.nseq == nseq && e.H == H && e.forward == forward &&
+          std::memcmp(e.t.cu, cu, (nseq + 1) * sizeof(int)) == 0 &&
+          std::memcmp(e.t.cuk, cuk, (nseq + 1) * sizeof(int)) == 0) {
+        e.used = ++clock_;
+        std::memcpy(out, &e.t, sizeof(VarlenTables));
+        *n_items = e.n_items;
+        *n_qtiles = e.n_qtiles;
+        ++stats_[3];
+        return;
+      }
+      if (e.used < victim->used) victim = &e;
+    }
+    build_tables(cu, cuk, nseq, H, forward, &victim->t, &victim->n_items, &victim->n_qtiles);
+    victim->nseq = nseq;
+    victim->H = H;
+    victim->forward = forward;
+    victim->used = ++clock_;
+    std::memcpy(out, &victim->t, sizeof(VarlenTables));
+    *n_items = victim->n_items;
+    *n_qtiles = victim->n_qtiles;
+    ++stats_[2];
+  }
+
+  // tensor-map encodes, tensor-map hits, table builds, table hits
+  void stats(long long* out) {
+    std::lock_guard<std::mutex> g(mu_);
+    for (int i = 0; i < 4; ++i) out[i] = stats_[i];
+  }
+
+ private:
+  struct MapKey {
+    const void* base;
+    int64_t d, heads, rows, head_stride, row_stride;
+    uint64_t box_rows;  // 64-bit so that the key has no padding bytes for memcmp
+  };
+  struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    uint64_t used = 0;  // 0: empty
+  };
+  struct TabEntry {
+    int nseq = 0, H = 0;
+    bool forward = false;
+    int n_items = 0, n_qtiles = 0;
+    VarlenTables t;
+    uint64_t used = 0;
+  };
+  std::mutex mu_;
+  MapEntry maps_[64];
+  TabEntry tabs_[8];
+  uint64_t clock_ = 0;
+  long long stats_[4] = {0, 0, 0, 0};
+};
+
+HostCache& host_cache() {
+  static HostCache* c = new HostCache();  // never destroyed: calls may come during exit
+  return *c;
+}
+
 struct Layout {
   int64_t q_row, k_row, v_row;   // element distance between token rows of q / k / v
   int64_t o_row;                 // ... of o and dO
@@ -198,6 +295,8 @@ std::atomic<int> g_sem_bias{0};
 // instrumentation; null = off).
 std::atomic<void*> g_prof_start{nullptr};
 std::atomic<void*> g_prof_stop{nullptr};
+// ... and around the preprocess and the dQ conversion kernels
+std::atomic<void*> g_prof_aux[4] = {{nullptr}, {nullptr}, {nullptr}, {nullptr}};
 
 }  // namespace
 
@@ -269,9 +368,10 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   const Layout lay = make_layout(layout, H, dqk, dv);
   const int64_t rows_q = varlen ? Tq : (int64_t)B * Tq;
   const int64_t rows_k = varlen ? Tk : (int64_t)B * Tk;
-  if (!make_panel_map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
-      !make_panel_map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
-      !make_panel_map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile))
+  HostCache& hc = host_cache();
+  if (!hc.map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
+      !hc.map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
+      !hc.map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile))
     return ATTN_ERR_CUDA;
   L.sh.nseq = B;
   L.sh.H = H;
@@ -291,7 +391,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if (rc) return rc;
   if (varlen) {
     int n_items = 0, n_qt = 0;
-    build_tables(cu_seqlens, cuk, B, H, true, &tables, &n_items, &n_qt);
+    hc.tables(cu_seqlens, cuk, B, H, true, &tables, &n_items, &n_qt);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
@@ -366,10 +466,11 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   const Layout lay = make_layout(layout, H, dqk, dv);
   const int64_t rows_q = varlen ? Tq : (int64_t)B * Tq;
   const int64_t rows_k = varlen ? Tk : (int64_t)B * Tk;
-  if (!make_panel_map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
-      !make_panel_map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
-      !make_panel_map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile) ||
-      !make_panel_map(&L.tm_do, dO, dv, H, rows_q, dv, lay.o_row, kTile))
+  HostCache& hc = host_cache();
+  if (!hc.map(&L.tm_q, q, dqk, H, rows_q, dqk, lay.q_row, kTile) ||
+      !hc.map(&L.tm_k, k, dqk, H, rows_k, dqk, lay.k_row, kTile) ||
+      !hc.map(&L.tm_v, v, dv, H, rows_k, dv, lay.v_row, kTile) ||
+      !hc.map(&L.tm_do, dO, dv, H, rows_q, dv, lay.o_row, kTile))
     return ATTN_ERR_CUDA;
   L.sh.nseq = B;
   L.sh.H = H;
@@ -389,7 +490,7 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   int n_qtiles;
   if (varlen) {
     int n_items = 0;
-    build_tables(cu_seqlens, cuk, B, H, false, &tables, &n_items, &n_qtiles);
+    hc.tables(cu_seqlens, cuk, B, H, false, &tables, &n_items, &n_qtiles);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
@@ -431,6 +532,7 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   L.sem_bias = g_sem_bias.load();
   L.prof_start = static_cast<cudaEvent_t>(g_prof_start.load());
   L.prof_stop = static_cast<cudaEvent_t>(g_prof_stop.load());
+  for (int e = 0; e < 4; ++e) L.prof_aux[e] = static_cast<cudaEvent_t>(g_prof_aux[e].load());
   const int sms = num_sms_current();
   if (sms <= 0) return ATTN_ERR_CUDA;
   L.num_sms = sms;
@@ -443,6 +545,22 @@ int attn_profile_main_kernel(void* event_start, void* event_stop) {
   if ((event_start == nullptr) != (event_stop == nullptr)) return ATTN_ERR_INVALID_ARG;
   g_prof_start.store(event_start);
   g_prof_stop.store(event_stop);
+  return ATTN_OK;
+}
+
+int attn_profile_aux_kernels(void* pre_start, void* pre_stop, void* convert_start,
+                             void* convert_stop) {
+  void* ev[4] = {pre_start, pre_stop, convert_start, convert_stop};
+  const bool any = ev[0] || ev[1] || ev[2] || ev[3];
+  const bool all = ev[0] && ev[1] && ev[2] && ev[3];
+  if (any && !all) return ATTN_ERR_INVALID_ARG;
+  for (int e = 0; e < 4; ++e) g_prof_aux[e].store(ev[e]);
+  return ATTN_OK;
+}
+
+int attn_debug_cache_stats(long long* out4) {
+  if (out4 == nullptr) return ATTN_ERR_INVALID_ARG;
+  host_cache().stats(out4);
   return ATTN_OK;
 }
 

@@ -971,11 +971,14 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     cfg.gridDim = dim3(L.num_sms * 4);
     cfg.blockDim = dim3(256);
     cfg.stream = L.stream;
-    cudaError_t e = cudaLaunchKernelEx(
+    cudaError_t e;
+    if (L.prof_aux[0] && (e = cudaEventRecord(L.prof_aux[0], L.stream)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(
         &cfg, attn_bwd_pre_kernel<DQK, DV, Tables>, reinterpret_cast<const __nv_bfloat16*>(L.o),
         reinterpret_cast<const __nv_bfloat16*>(L.dout), L.lse, L.o_row_stride, L.do_row_stride,
         L.lse_head_stride, L.lse_seq_stride, total_rows, L.n_qtiles, L.ws, L.sh, tb);
     if (e != cudaSuccess) return e;
+    if (L.prof_aux[1] && (e = cudaEventRecord(L.prof_aux[1], L.stream)) != cudaSuccess) return e;
   }
   // 2. main
   {
@@ -1018,9 +1021,11 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
+    if (L.prof_aux[2] && (e = cudaEventRecord(L.prof_aux[2], L.stream)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, k, static_cast<const float*>(L.ws.dq_acc),
                            reinterpret_cast<__nv_bfloat16*>(L.dq), L.dq_row_stride, L.scale, L.sh, tb);
     if (e != cudaSuccess) return e;
+    if (L.prof_aux[3] && (e = cudaEventRecord(L.prof_aux[3], L.stream)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }

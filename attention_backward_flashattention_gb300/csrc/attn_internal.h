@@ -54,6 +54,7 @@ struct BwdLaunch {
   int deterministic;
   int sem_bias;       // fault injection for tests (0 in normal use)
   cudaEvent_t prof_start, prof_stop;  // recorded around the main kernel when set
+  cudaEvent_t prof_aux[4];            // around the preprocess (0, 1) and dQ conversion (2, 3)
   BwdWorkspace ws;
   SeqShape sh;        // n_items = kv-tile items
   const VarlenTables* tables;

@@ -2,15 +2,24 @@
 
 One step = the whole hot path on one batch of synthetic bf16 input: forward
 (O, LSE) then backward (preprocess, main kernel, dQ conversion), all through
-the C ABI.  The workload is causal, H=16, d=128, T=32768, B=1 (32K tokens).
-`value` = backward FLOPs 2*B*H*T^2*(3*dqk+2*dv)/2 / backward time, summed over
-ranks.  Inputs (5 x 134 MB) exceed the 126 MB L2, so no flush is needed
-between steps.
+the C ABI.  The default workload is causal, H=16, d=128, T=32768, B=1 (32K
+tokens); `--workload` names any other (the GPT-2-shaped packed layer, the
+sweep, the (192,128) points, the variable-length deterministic batch).
+`value` = backward FLOPs 2*B*H*T^2*(3*dqk+2*dv)/2 (per sequence for a
+variable-length batch) / backward time, summed over ranks.  Inputs of the
+32K-token workloads (5 x 134 MB) exceed the 126 MB L2, so no flush is needed
+between steps.  The same line carries the inference-mode forward
+(`fwd_inference`), the time of the other dQ reduction mode (deterministic or
+fast), the HBM rates of the two memory-bound kernels (`aux_kernels`) and the
+end-to-end figure through host buffers (`e2e`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
 
---impl reference times the fp64 CPU oracle (the reference arm for this
-workload) on a bounded sample of the same workload, on the host cores.
+--gpus N without a launcher starts N ranks itself (replicas, one per GPU);
+under torchrun it must match WORLD_SIZE.  --impl reference times the fp64 CPU
+oracle (the reference arm for this workload) on a bounded sample of the same
+workload, on the host cores.
 """
 from __future__ import annotations
 
@@ -32,6 +41,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+from attention_backward_flashattention_gb300 import binding  # noqa: E402
 from attention_backward_flashattention_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "attn bwd TFLOP/s (bf16, causal, d=128, 32K tok) and % of GB300 BF16 peak"
@@ -50,9 +60,13 @@ def _peaks():
 
 
 def _config(w, extra=None):
+    tensor_mb = w.total_tokens * w.H * w.dqk * 2 / 1e6
+    l2 = (f"inputs larger than L2 (5 x {tensor_mb:.0f} MB bf16), no flush" if tensor_mb * 5 > 130
+          else f"inputs ({5 * tensor_mb:.0f} MB) fit in L2: steps re-read them from L2")
     c = {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dqk": w.dqk, "dv": w.dv,
-         "causal": w.causal, "layout": "BTHD", "deterministic": w.deterministic,
-         "l2": "inputs larger than L2 (5 x 134 MB bf16), no flush"}
+         "causal": w.causal, "layout": "packed (B,T,3,H,d)" if w.layout == syn.LAYOUT_PACKED
+         else ("varlen (sum T,H,d)" if w.varlen else "BTHD"),
+         "deterministic": w.deterministic, "l2": l2}
     if extra:
         c.update(extra)
     return c
@@ -124,17 +138,60 @@ def kernel_sources_sha256():
     return h.hexdigest()
 
 
-def _traffic_for(kernel_name):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    sources are unchanged since the counters were taken; else None."""
+def _ncu_record(kernel_name, workload):
+    """The committed ncu counters of `kernel_name` on `workload`
+    (profiles/ncu_traffic.json, keyed by kernel, then workload) when the
+    kernel's sources are unchanged since they were taken; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel_name)
+        rec = json.load(f).get(kernel_name, {}).get(workload)
     if not rec or rec.get("sources_sha256") != kernel_sources_sha256():
         return None
-    return rec.get("bytes_per_launch")
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# workload plumbing (layouts, problems, byte counts)
+# ---------------------------------------------------------------------------
+def _cu(w):
+    return None if not w.varlen else [0] + list(np.cumsum(w.varlen).astype(int))
+
+
+def _lengths(w):
+    return list(w.varlen) if w.varlen else [w.T] * w.B
+
+
+def _q_tiles(w):
+    return sum(-(-L // 128) for L in _lengths(w))
+
+
+def aux_bytes(w):
+    """Bytes the backward's two memory-bound kernels move per launch.
+
+    preprocess: reads O and dO (bf16) and LSE, writes -D and -LSE*log2(e) per
+    padded query row (fp32) and zeroes the fp32 dQ accumulator;
+    'algorithmic' counts only the reads and the D / LSE writes (the operation
+    D = rowsum(dO * O)), 'moved' adds the accumulator's zeroing.
+    dQ conversion: reads the fp32 accumulator, writes bf16 dQ."""
+    rows = w.total_tokens
+    padded = _q_tiles(w) * 128
+    H = w.H
+    pre_alg = rows * H * (2 * w.dv * 2 + 4) + 2 * padded * H * 4
+    pre_moved = pre_alg + padded * H * w.dqk * 4
+    cvt = padded * H * w.dqk * 4 + rows * H * w.dqk * 2
+    return {"pre_algorithmic": pre_alg, "pre_moved": pre_moved, "convert": cvt}
+
+
+def _problems(t, cu):
+    """(B,T,H,d) or (sum T,H,d) tensor -> list of float64 [T][d] per (sequence, head)."""
+    t = t.float()
+    if cu is None:
+        x = t.permute(0, 2, 1, 3).contiguous()
+        return list(x.reshape(-1, x.shape[2], x.shape[3]).double().numpy())
+    return [t[cu[s]:cu[s + 1], h, :].double().numpy()
+            for s in range(len(cu) - 1) for h in range(t.shape[1])]
 
 
 # ---------------------------------------------------------------------------
@@ -142,29 +199,26 @@ def _traffic_for(kernel_name):
 # ---------------------------------------------------------------------------
 def oracle_sample(w, rows_per_head, seed=0, x=None):
     """Time the oracle's row-by-row backward on `rows_per_head` random query
-    rows of every head of `w` (one OpenMP thread per head).  Returns
-    (TFLOP/s in the metric's FLOP convention, seconds, threads, description)."""
+    rows of every (sequence, head) problem of `w` (one OpenMP thread per
+    problem).  Returns (TFLOP/s in the metric's FLOP convention, seconds,
+    threads, description)."""
     import oracle
     oracle.build()
     if x is None:
         x = syn.make_inputs(w)
-
-    def heads(t):
-        t = t.float().permute(0, 2, 1, 3).contiguous()
-        return list(t.reshape(-1, t.shape[2], t.shape[3]).double().numpy())
-
-    q, k, v, dO = (heads(x[n]) for n in ("q", "k", "v", "dO"))
+    cu = _cu(w)
+    q, k, v, dO = (_problems(x[n], cu) for n in ("q", "k", "v", "dO"))
     rng = np.random.default_rng(seed)
-    rows = [np.sort(rng.choice(w.T, size=rows_per_head, replace=False)).astype(np.int32)
-            for _ in q]
+    rows = [np.sort(rng.choice(len(a), size=min(rows_per_head, len(a)), replace=False))
+            .astype(np.int32) for a in q]
     per = 2.0 * (3 * w.dqk + 2 * w.dv)
-    flops = sum(per * ((r + 1).sum() if w.causal else w.T * len(r)) for r in rows)
+    flops = sum(per * ((r + 1).sum() if w.causal else len(a) * len(r)) for r, a in zip(rows, q))
     t0 = time.perf_counter()
     oracle.backward(q, k, v, dO, w.causal, w.scale, rows=rows)
     dt = time.perf_counter() - t0
     desc = (f"oracle row-by-row backward (recomputes each row's forward), {rows_per_head} "
-            f"random query rows x {len(q)} heads of {w.name}; FLOPs counted as the rows' share "
-            f"of 2*H*T^2*(3*dqk+2*dv)/2")
+            f"random query rows x {len(q)} (sequence, head) problems of {w.name}; FLOPs "
+            f"counted as the rows' share of 2*H*T^2*(3*dqk+2*dv)/2")
     return flops / dt / 1e12, dt, oracle.num_threads(), desc
 
 
@@ -182,45 +236,163 @@ def job_tflops(flops_per_rank, world, steps, seconds):
     return world * flops_per_rank * steps / seconds / 1e12
 
 
+def peak_for(peaks, timed_region_s):
+    """The bf16 denominator for a kernel timed inside a region of this length:
+    the burst figure below 2 s (the cuBLAS burst is a short loop too), the
+    sustained one (measured over seconds under the power cap) above."""
+    if timed_region_s < 2.0:
+        return peaks["bf16_burst"], f"bf16 burst ({peaks['source']}; timed region " \
+                                    f"{timed_region_s:.2f} s < 2 s)"
+    return peaks["bf16_sustained"], f"bf16 sustained ({peaks['source']}; timed region " \
+                                    f"{timed_region_s:.2f} s)"
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, rank, world):
-    from attention_backward_flashattention_gb300 import binding
+class Problem:
+    """Device tensors of one workload in its own layout, and the C-ABI calls
+    of its forward and backward (argument marshalling only)."""
 
+    def __init__(self, w, x, dev):
+        self.w = w
+        self.cu = _cu(w)
+        self.varlen = self.cu is not None
+        B, H, dqk, dv = w.B, w.H, w.dqk, w.dv
+        self.Tq = w.total_tokens if self.varlen else w.T
+        if w.layout == syn.LAYOUT_PACKED:
+            self.qkv = x["qkv"].to(dev)
+            self.q, self.k, self.v = (self.qkv.select(-3, i) for i in range(3))
+            self.gqkv = torch.empty_like(self.qkv)
+            self.dq, self.dk, self.dv = (self.gqkv.select(-3, i) for i in range(3))
+        else:
+            self.q, self.k, self.v = (x[n].to(dev) for n in ("q", "k", "v"))
+            self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+        self.dO = x["dO"].to(dev)
+        lead = (self.Tq,) if self.varlen else (B, w.T)
+        self.o = torch.empty(*lead, H, dv, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(*((H, self.Tq) if self.varlen else (B, H, w.T)),
+                               dtype=torch.float32, device=dev)
+        self.ws_bytes = binding.attn_bwd_workspace_size(B, H, self.Tq, self.Tq, dqk, dv,
+                                                        self.varlen, True)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def fwd(self, stream, with_lse=True):
+        w = self.w
+        rc = binding.attn_fwd(self.q, self.k, self.v, self.o, self.lse if with_lse else None,
+                              w.B, w.H, self.Tq, self.Tq, w.dqk, w.dv, w.causal, w.scale,
+                              self.cu, w.layout, stream)
+        assert rc == 0, rc
+
+    def bwd(self, stream, deterministic):
+        w = self.w
+        rc = binding.attn_bwd(self.q, self.k, self.v, self.o, self.dO, self.lse, self.dq,
+                              self.dk, self.dv, w.B, w.H, self.Tq, self.Tq, w.dqk, w.dv,
+                              w.causal, w.scale, self.cu, w.layout, deterministic, self.ws,
+                              self.ws_bytes, stream)
+        assert rc == 0, rc
+
+    def status_ok(self):
+        return binding.attn_bwd_status(self.ws) == 0 and binding.attn_fwd_status() == 0
+
+
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _time_loop(stream, steps, body):
+    """Device time (ms) of `steps` calls of body(), CUDA events on `stream`."""
+    a, b = _events(2)
+    a.record(stream)
+    for _ in range(steps):
+        body()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def e2e_step_host(args, w, x, dev, stream, K):
+    """Host tensors in, gradients out, through attn_step_host (fixed-length
+    (B,T,H,d) only): ms per step and the bytes copied each way."""
+    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dO"))
+    hdq, hdk, hdv = (torch.empty(x[n].shape, dtype=torch.bfloat16, pin_memory=True)
+                     for n in ("q", "k", "v"))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+    G = args.e2e_heads_per_group
+    scratch_bytes = binding.attn_step_host_scratch_size(B, H, T, dqk, dv, G, w.deterministic)
+    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=dev)
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    stream2 = torch.cuda.Stream(dev) if args.e2e_streams == 2 else None
+
+    def step():
+        rc = binding.attn_step_host(hq, hk, hv, hdo, None, hdq, hdk, hdv, B, H, T, dqk, dv,
+                                    w.causal, w.scale, w.deterministic, G, scratch,
+                                    scratch_bytes, stream, stream2, h2d_stream, d2h_stream)
+        assert rc == 0, rc
+
+    step()
+    torch.cuda.synchronize()
+    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+        raise RuntimeError("device status error in the e2e warm-up")
+    ms = _time_loop(stream, K, step) / K
+    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+        raise RuntimeError("device status error in the e2e region")
+    api = ("attn_step_host (pinned host tensors; forward + backward; copies of one head group "
+           "overlap the kernels of another)")
+    return ms, h2d, d2h, api, {"heads_per_group": G or -(-H // 2),
+                               "compute_streams": args.e2e_streams}
+
+
+def e2e_copies(w, x, prob, stream, K):
+    """Layouts attn_step_host does not take (packed QKV, variable length):
+    pinned host inputs copied in, attn_fwd + attn_bwd, gradients copied out,
+    all on one stream."""
+    names = ("qkv", "dO") if w.layout == syn.LAYOUT_PACKED else ("q", "k", "v", "dO")
+    host_in = [x[n].contiguous().pin_memory() for n in names]
+    dev_in = [prob.qkv, prob.dO] if w.layout == syn.LAYOUT_PACKED else \
+        [prob.q, prob.k, prob.v, prob.dO]
+    dev_out = [prob.gqkv] if w.layout == syn.LAYOUT_PACKED else [prob.dq, prob.dk, prob.dv]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            prob.fwd(stream)
+            prob.bwd(stream, w.deterministic)
+            for d, h in zip(dev_out, host_out):
+                h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    ms = _time_loop(stream, K, step) / K
+    if not prob.status_ok():
+        raise RuntimeError("device status error in the e2e region")
+    return ms, h2d, d2h, "pinned host copies in, attn_fwd + attn_bwd, gradients out (one stream)", {}
+
+
+def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     w = WORKLOAD
     x = syn.make_inputs(w)
-    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
-    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
-    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
-    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    need = binding.attn_bwd_workspace_size(B, H, T, T, dqk, dv, False, w.deterministic)
-    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    prob = Problem(w, x, dev)
     stream = torch.cuda.current_stream()
-
-    def fwd():
-        rc = binding.attn_fwd(q, k, v, o, lse, B, H, T, T, dqk, dv, w.causal, w.scale, None, 0,
-                              stream)
-        assert rc == 0, rc
-
-    def bwd():
-        rc = binding.attn_bwd(q, k, v, o, dO, lse, dq, dk, dvv, B, H, T, T, dqk, dv, w.causal,
-                              w.scale, None, 0, w.deterministic, ws, need, stream)
-        assert rc == 0, rc
-
+    det = w.deterministic
     launches_per_step = 1 + 3
     for _ in range(args.warmup):
-        fwd()
-        bwd()
+        prob.fwd(stream)
+        prob.bwd(stream, det)
     torch.cuda.synchronize()
-    if binding.attn_bwd_status(ws) != 0 or binding.attn_fwd_status() != 0:
+    if not prob.status_ok():
         raise RuntimeError("device status error during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    ev = [_events(9) for _ in range(K)]
     for e in ev:       # create the events before the timed region
         for z in e:
             z.record(stream)
@@ -232,104 +404,113 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start, t_stop = _events(2)
     t_start.record(stream)
     for i in range(K):
         e = ev[i]
         e[0].record(stream)
-        fwd()
+        prob.fwd(stream)
         e[1].record(stream)
         binding.attn_profile_main_kernel(e[3], e[4])
-        bwd()
+        binding.attn_profile_aux_kernels(e[5], e[6], e[7], e[8])
+        prob.bwd(stream, det)
         e[2].record(stream)
     t_stop.record(stream)
     torch.cuda.synchronize()
     binding.attn_profile_main_kernel(None, None)
+    binding.attn_profile_aux_kernels(None, None, None, None)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if rank == 0 else None
     total_ms = t_start.elapsed_time(t_stop)
-    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    main_ms = [ev[i][3].elapsed_time(ev[i][4]) for i in range(K)]
-    if binding.attn_bwd_status(ws) != 0 or binding.attn_fwd_status() != 0:
+    sums = [sum(ev[i][a].elapsed_time(ev[i][b]) for i in range(K))
+            for a, b in ((0, 1), (1, 2), (3, 4), (5, 6), (7, 8))]
+    if not prob.status_ok():
         raise RuntimeError("device status error in the timed region")
 
-    # e2e: pinned host inputs -> device, forward + backward, gradients -> host, through the
-    # host-buffer entry point (copies of one head group overlap the kernels of another)
-    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dO"))
-    hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v))
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
-    G = args.e2e_heads_per_group
-    scratch_bytes = binding.attn_step_host_scratch_size(B, H, T, dqk, dv, G, w.deterministic)
-    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=dev)
-    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    stream2 = torch.cuda.Stream(dev) if args.e2e_streams == 2 else None
+    # inference-mode forward (lse = NULL) and the other dQ reduction mode
+    inf_ms = _time_loop(stream, K, lambda: prob.fwd(stream, with_lse=False))
+    Kd = min(K, 10)
+    other_ms = _time_loop(stream, Kd, lambda: prob.bwd(stream, not det))
+    if not prob.status_ok():
+        raise RuntimeError("device status error in the extra timings")
 
-    def e2e_step():
-        rc = binding.attn_step_host(hq, hk, hv, hdo, None, hdq, hdk, hdv, B, H, T, dqk, dv,
-                                    w.causal, w.scale, w.deterministic, G, scratch,
-                                    scratch_bytes, stream, stream2, h2d_stream, d2h_stream)
-        assert rc == 0, rc
+    if w.layout == syn.LAYOUT_BTHD and not w.varlen:
+        e2e_ms, h2d, d2h, api, e2e_extra = e2e_step_host(args, w, x, dev, stream, K)
+    else:
+        e2e_ms, h2d, d2h, api, e2e_extra = e2e_copies(w, x, prob, stream, K)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
-        raise RuntimeError("device status error in the e2e warm-up")
-    if world > 1:
-        torch.distributed.barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(K):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / K
-    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
-        raise RuntimeError("device status error in the e2e region")
-
-    total_ms, bwd_sum, fwd_sum, main_sum, e2e_ms = max_over_ranks(
-        [total_ms, sum(bwd_ms), sum(fwd_ms), sum(main_ms), e2e_ms], world, dev)
+    total_ms, fwd_sum, bwd_sum, main_sum, pre_sum, cvt_sum, inf_ms, other_ms, e2e_ms = \
+        max_over_ranks([total_ms, *sums, inf_ms, other_ms, e2e_ms], world, dev)
     if rank != 0:
         return None
 
     peaks = _peaks()
-    bwd_flops = w.bwd_flops()
-    fwd_flops = w.fwd_flops()
+    bwd_flops, fwd_flops = w.bwd_flops(), w.fwd_flops()
     value = job_tflops(bwd_flops, world, K, bwd_sum * 1e-3)
     main_avg_s = main_sum / K * 1e-3
     achieved = bwd_flops / main_avg_s / 1e12
-    peak = peaks["bf16_sustained"]
-    traffic = _traffic_for("attn_bwd_main_kernel")
+    timed_region_s = total_ms * 1e-3
+    peak, peak_kind = peak_for(peaks, timed_region_s)
+    rec = _ncu_record("attn_bwd_main_kernel", w.name)
+    nb = aux_bytes(w)
+    pre_s, cvt_s = pre_sum / K * 1e-3, cvt_sum / K * 1e-3
+    aux = {
+        "attn_bwd_pre_kernel": {
+            "avg_ms": pre_s * 1e3, "bytes_moved": nb["pre_moved"],
+            "bytes_algorithmic": nb["pre_algorithmic"],
+            "gbs": nb["pre_moved"] / pre_s / 1e9,
+            "frac_of_hbm": nb["pre_moved"] / pre_s / 1e9 / peaks["hbm"],
+            "gbs_algorithmic": nb["pre_algorithmic"] / pre_s / 1e9},
+        "attn_bwd_convert_kernel": {
+            "avg_ms": cvt_s * 1e3, "bytes_moved": nb["convert"],
+            "gbs": nb["convert"] / cvt_s / 1e9,
+            "frac_of_hbm": nb["convert"] / cvt_s / 1e9 / peaks["hbm"]},
+        "hbm_peak_gbs": peaks["hbm"], "unit": "GB/s",
+        "bytes": "moved = every byte the kernel reads or writes as built (the preprocess also "
+                 "zeroes the fp32 dQ accumulator); algorithmic = O, dO, LSE read and D written",
+    }
+    inf_per = fwd_flops / (inf_ms / K * 1e-3) / 1e12
+    fwd_inf = {"value": world * inf_per, "unit": UNIT, "ms": inf_ms / K,
+               "frac_of_burst": inf_per / peaks["bf16_burst"],
+               "mode": "attn_fwd with lse = NULL (inference: no statistics written)"}
+    det_key = "bwd_fast_ms" if det else "bwd_deterministic_ms"
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         tf, secs, cores, desc = oracle_sample(w, args.cpu_rows, x=x)
         cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
+    extra = {"parallelism": f"replicas x{world} (independent heads, no exchange)"}
+    if w.varlen:
+        extra["seqlens"] = list(w.varlen)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": _config(w, {"parallelism": f"replicas x{world} (independent heads, no exchange)"}),
+        "config": _config(w, extra),
         "pct_of_bf16_peak": {"burst": 100.0 * value / world / peaks["bf16_burst"],
                              "sustained": 100.0 * value / world / peaks["bf16_sustained"],
                              "peaks": peaks["source"]},
         "bwd_ms": bwd_sum / K, "fwd_ms": fwd_sum / K,
         "fwd_tflops": world * fwd_flops * K / (fwd_sum * 1e-3) / 1e12,
+        "fwd_inference": fwd_inf,
+        det_key: other_ms / Kd,
+        "deterministic_cost_pct": 100.0 * ((bwd_sum / K) / (other_ms / Kd) - 1.0) if det else
+        100.0 * ((other_ms / Kd) / (bwd_sum / K) - 1.0),
         "roofline": {"kernel": "attn_bwd_main_kernel", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "peak_kind": peak_kind,
                      "frac_of_burst": achieved / peaks["bf16_burst"],
-                     "traffic": traffic, "algorithmic_flops_per_launch": bwd_flops,
+                     "frac_of_sustained": achieved / peaks["bf16_sustained"],
+                     "traffic": None if rec is None else rec["bytes_per_launch"],
+                     "tensor_pipe_pct_ncu": None if rec is None else rec.get("tensor_pipe_pct"),
+                     "algorithmic_flops_per_launch": bwd_flops,
                      "avg_launch_ms": main_avg_s * 1e3},
+        "aux_kernels": aux,
         "cpu_baseline": cpu,
         "e2e": {"value": world * bwd_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "api": "attn_step_host (pinned host tensors; forward + backward; copies of "
-                       "one head group overlap the kernels of another)",
-                "heads_per_group": G or -(-H // 2), "compute_streams": args.e2e_streams},
+                "api": api, **e2e_extra},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
     }
@@ -337,26 +518,17 @@ def run_ours(args, rank, world):
 
 
 def run_fwd_only(args, rank, world):
-    """Inference-mode forward (lse=NULL) of the workload: forward TFLOP/s.
-    A separate measurement (not the bwd headline): `--fwd-only`."""
-    from attention_backward_flashattention_gb300 import binding
-
+    """Inference-mode forward (lse=NULL) of the workload alone: forward TFLOP/s.
+    A separate measurement (`--fwd-only`); the default line carries the same
+    figure as `fwd_inference`."""
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     w = WORKLOAD
     x = syn.make_inputs(w)
-    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
-    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    prob = Problem(w, x, dev)
     stream = torch.cuda.current_stream()
-
-    def fwd():
-        rc = binding.attn_fwd(q, k, v, o, None, B, H, T, T, dqk, dv, w.causal, w.scale, None, 0,
-                              stream)
-        assert rc == 0, rc
-
     for _ in range(args.warmup):
-        fwd()
+        prob.fwd(stream, with_lse=False)
     torch.cuda.synchronize()
     K = args.steps
     sampler = ClockSampler()
@@ -366,30 +538,25 @@ def run_fwd_only(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(K):
-        fwd()
-    b.record(stream)
-    torch.cuda.synchronize()
+    total_ms = _time_loop(stream, K, lambda: prob.fwd(stream, with_lse=False))
     clocks = sampler.stop() if rank == 0 else None
     if binding.attn_fwd_status() != 0:
         raise RuntimeError("device status error in the timed region")
-    (total_ms,) = max_over_ranks([a.elapsed_time(b)], world, dev)
+    (total_ms,) = max_over_ranks([total_ms], world, dev)
     if rank != 0:
         return None
     peaks = _peaks()
     flops = w.fwd_flops()
     value = job_tflops(flops, world, K, total_ms * 1e-3)
     per = flops / (total_ms / K * 1e-3) / 1e12
+    peak, peak_kind = peak_for(peaks, total_ms * 1e-3)
     return {
         "metric": "attn fwd TFLOP/s (bf16, inference: no LSE)", "value": value, "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": _config(w, {"mode": "forward only, lse=NULL"}),
         "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": per,
-                     "peak": peaks["bf16_sustained"], "unit": UNIT,
-                     "frac": per / peaks["bf16_sustained"],
+                     "peak": peak, "unit": UNIT, "frac": per / peak, "peak_kind": peak_kind,
                      "frac_of_burst": per / peaks["bf16_burst"], "traffic": None,
                      "algorithmic_flops_per_launch": flops},
         "gpu_launches": K, "clocks": clocks,
@@ -421,11 +588,11 @@ def run_block_sparse(args, rank, world):
     """Forward + backward of the workload under a random block mask of the
     given density (`--block-density`): TFLOP/s over the visible pairs only.
     A separate measurement (not the headline line)."""
-    from attention_backward_flashattention_gb300 import binding
-
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     w = WORKLOAD
+    if w.varlen or w.layout != syn.LAYOUT_BTHD:
+        raise ValueError("the block-sparse bench takes fixed-length (B,T,H,d) workloads")
     if w.T % 128:
         raise ValueError("block-sparse bench wants T a multiple of 128")
     x = syn.make_inputs(w)
@@ -497,8 +664,10 @@ def run_block_sparse(args, rank, world):
                               "dense_bwd_flops": w.bwd_flops()}),
         "fwd_tflops": job_tflops(fwd_flops, world, K, fwd_ms * 1e-3), "fwd_ms": fwd_ms / K,
         "roofline": {"kernel": "attn_bwd (pre + main + convert)", "bound": "tensor",
-                     "achieved": per, "peak": peaks["bf16_sustained"], "unit": UNIT,
-                     "frac": per / peaks["bf16_sustained"], "traffic": None,
+                     "achieved": per, "peak": peak_for(peaks, (fwd_ms + bwd_ms) * 1e-3)[0],
+                     "unit": UNIT,
+                     "frac": per / peak_for(peaks, (fwd_ms + bwd_ms) * 1e-3)[0],
+                     "peak_kind": peak_for(peaks, (fwd_ms + bwd_ms) * 1e-3)[1], "traffic": None,
                      "algorithmic_flops_per_launch": bwd_flops},
         "gpu_launches": 4 * K, "clocks": clocks,
     }
@@ -533,6 +702,20 @@ def run_reference(args, rank, world):
     }
 
 
+def launch_ranks(n):
+    """`--gpus N` without a launcher: start N ranks of this command under
+    torch.distributed.run (one process per GPU, rendezvous on 127.0.0.1) and
+    return their exit status."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     global WORKLOAD
     ap = argparse.ArgumentParser()
@@ -542,7 +725,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--workload", default=syn.HEADLINE.name,
-                    help="fixed-length workload name (profiling runs on smaller cases)")
+                    help="workload name: " + ", ".join(syn.ALL))
     ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per head per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-heads-per-group", type=int, default=0,
@@ -554,12 +737,20 @@ def main():
     ap.add_argument("--block-density", type=float, default=0.0,
                     help="time forward + backward under a random block mask of this density")
     args = ap.parse_args()
+    if args.workload not in syn.ALL:
+        ap.error(f"unknown workload {args.workload!r}")
     WORKLOAD = syn.ALL[args.workload]
-    if WORKLOAD.varlen or WORKLOAD.layout != syn.LAYOUT_BTHD:
-        ap.error("bench workloads are fixed-length (B,T,H,d)")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        sys.exit(launch_ranks(args.gpus))
+    world = int(env_world or "1")
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        sys.exit(2)
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
         backend = "nccl" if args.impl == "ours" else "gloo"

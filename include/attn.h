@@ -212,17 +212,25 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
  * the workspace: the library's own 32 MiB device array stands in for it, so
  * it needs attn_bwd_workspace_size() <= 32 MiB (larger problems return
  * ATTN_ERR_SCRATCH_TOO_SMALL; e.g. B=8, H=12, T=1024, d=64 fits).  The first
- * call on each device looks up the array's address (make it before any stream
- * capture); every device that loads this code holds the array until exit.
- * All calls share the array: calls that overlap on the GPU race, so order
- * them on one stream.  Device-side timeouts of these calls are not
- * reported (there is no caller-visible workspace to read them from).  No
- * counterpart on the pages.
+ * call in each CUDA context looks up the array's address (make it before any
+ * stream capture); a call after the device's context was reset and
+ * re-created looks it up again.  Every device that loads this code holds the
+ * array until exit.  All calls share the array: calls that overlap on the GPU
+ * race, so order them on one stream.  A device-side timeout of the last call
+ * is read with attn_bwd_noalloc_status().  No counterpart on the pages.
  */
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                      const float* lse, void* dq, void* dk, void* dv_out, int B, int H, int Tq,
                      int Tk, int dqk, int dv, int causal, float scale, const int* cu_seqlens,
                      int layout, int deterministic, void* stream);
+
+/*
+ * Synchronises `stream` and returns the device status of the last
+ * attn_bwd_noalloc call on the current device (ATTN_OK or ATTN_ERR_TIMEOUT),
+ * read from the library's scratch array; allocates nothing.  No counterpart
+ * on the pages.
+ */
+int attn_bwd_noalloc_status(void* stream);
 
 /*
  * Synchronises `stream` and returns the device status of the last backward
@@ -245,6 +253,28 @@ int attn_fwd_status(void* stream);
  * counterpart on the pages.
  */
 int attn_profile_main_kernel(void* event_start, void* event_stop);
+
+/*
+ * Instrumentation, like attn_profile_main_kernel: when all four are non-NULL
+ * (cudaEvent_t handles), every later attn_bwd call records pre_start and
+ * pre_stop around its preprocess kernel (D and the per-row statistics) and
+ * convert_start and convert_stop around its dQ conversion kernel.  Four NULLs
+ * turn it off; a mix returns ATTN_ERR_INVALID_ARG.  Benchmark support (the
+ * HBM rates of the two memory-bound kernels); no counterpart on the pages.
+ */
+int attn_profile_aux_kernels(void* pre_start, void* pre_stop, void* convert_start,
+                             void* convert_stop);
+
+/*
+ * Counters of the library's host-side cache (TMA tensor maps and the
+ * schedule tables of variable-length batches, reused across calls with the
+ * same pointers, shapes and options): out4[0] tensor maps encoded, out4[1]
+ * tensor maps reused, out4[2] tables built, out4[3] tables reused, since the
+ * library was loaded.  Returns ATTN_ERR_INVALID_ARG for NULL.  Test and
+ * diagnostics support; the cache itself follows the build-once, run-many
+ * graphs of "ops(8)..." §1.3.
+ */
+int attn_debug_cache_stats(long long* out4);
 
 /*
  * Test hook (host-side fault injection; 0 = normal operation): every ordered

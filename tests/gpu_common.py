@@ -7,13 +7,21 @@ import torch
 import oracle
 from attention_backward_flashattention_gb300 import binding
 from attention_backward_flashattention_gb300 import synthetic as syn
-from tests._common import max_abs, rel_err
+from tests._common import max_abs, rel_err, row_err
 
 # Tolerances (bf16 inputs, fp32 accumulation): normwise relative error for
 # O and for dQ/dK/dV, maximum absolute error for the natural-log LSE.
 TOL_O = 5e-3
 TOL_GRAD = 1e-2
 TOL_LSE = 1e-4
+# Per row of O, dQ, dK, dV (beside the normwise bounds): the error norm of a
+# row may be at most 5 % of that row's norm (or of the rms row norm, for rows
+# whose exact values are near zero), so a single wrong row or tile cannot hide
+# in a whole-tensor norm.  A CPU model of the kernels' bf16 rounding points
+# (P, dP - D, dS, O before D, the outputs) reproduces the GPU's errors and puts
+# the worst row of 36 seeded problem sets at 2.8e-2 for dQ (short causal rows,
+# whose dS entries cancel) and below 1e-2 for O, dK and dV.
+TOL_ROW = 5e-2
 
 
 def run_gpu(x, w, deterministic=None, with_lse=True, window=None):
@@ -83,8 +91,12 @@ def compare_full(x, w, g, pick=None, window=None, block_mask=None):
     gp = {key: sel(problems(g[key], w, cu)) for key in ("O", "dQ", "dK", "dV")}
     gl = sel(lse_problems(g["LSE"], w, cu))
     cat = lambda a: np.concatenate([np.asarray(z).reshape(-1) for z in a])
-    err = {key: rel_err(cat(gp[key]), cat(r[key] if isinstance(r[key], list) else list(r[key])))
-           for key in ("O", "dQ", "dK", "dV")}
+    rows = lambda a: np.concatenate([np.asarray(z).reshape(-1, np.asarray(z).shape[-1])
+                                     for z in a])
+    as_list = lambda a: a if isinstance(a, list) else list(a)
+    err = {key: rel_err(cat(gp[key]), cat(as_list(r[key]))) for key in ("O", "dQ", "dK", "dV")}
+    for key in ("O", "dQ", "dK", "dV"):
+        err[key + "_row"] = row_err(rows(gp[key]), rows(as_list(r[key])))
     ref_lse = cat(r["LSE"] if isinstance(r["LSE"], list) else list(r["LSE"]))
     got_lse = cat(gl)
     empty = np.isneginf(ref_lse)
@@ -131,13 +143,33 @@ def compare_sampled(x, w, g, heads, n_rows=48, kv_heads=(), seed=0):
     for key, (a, b) in acc.items():
         if not a:
             continue
+        if key != "LSE":
+            err[key + "_row"] = row_err(np.concatenate([z.reshape(-1, z.shape[-1]) for z in a]),
+                                        np.concatenate([z.reshape(-1, z.shape[-1]) for z in b]))
         a = np.concatenate([z.reshape(-1) for z in a])
         b = np.concatenate([z.reshape(-1) for z in b])
         err[key] = max_abs(a, b) if key == "LSE" else rel_err(a, b)
     return err
 
 
+def compare_forward_sampled(x, w, o, heads, n_rows=48, seed=0):
+    """O of the inference-mode forward (no LSE) at sampled query rows of
+    `heads`, against the oracle's forward computed row by row."""
+    (q, k, v, _), cu = inputs_as_problems(x, w)
+    go = problems(o, w, cu)
+    got, ref = [], []
+    for p in heads:
+        rows = sample_rows(q[p].shape[0], n_rows, seed + p)
+        r = oracle.backward([q[p]], [k[p]], [v[p]], [np.zeros((q[p].shape[0], v[p].shape[1]))],
+                            w.causal, w.scale, rows=[rows])
+        got.append(go[p][rows])
+        ref.append(np.asarray(r["O"])[0][rows])
+    a, b = np.concatenate(got), np.concatenate(ref)
+    return {"O": rel_err(a.reshape(-1), b.reshape(-1)), "O_row": row_err(a, b)}
+
+
 def assert_within(err, where=""):
-    limits = {"O": TOL_O, "dQ": TOL_GRAD, "dK": TOL_GRAD, "dV": TOL_GRAD, "LSE": TOL_LSE}
+    limits = {"O": TOL_O, "dQ": TOL_GRAD, "dK": TOL_GRAD, "dV": TOL_GRAD, "LSE": TOL_LSE,
+              "O_row": TOL_ROW, "dQ_row": TOL_ROW, "dK_row": TOL_ROW, "dV_row": TOL_ROW}
     bad = {k: v for k, v in err.items() if not (v <= limits[k])}
     assert not bad, f"{where}: {err}"

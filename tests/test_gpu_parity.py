@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_backward_flashattention_gb300 import binding
 from attention_backward_flashattention_gb300 import synthetic as syn
 
@@ -168,20 +169,36 @@ def test_gpt2_packed_every_element():
     gc.assert_within(gc.compare_full(x, w, g), w.name)
 
 
-@pytest.mark.parametrize("w", [w for w in syn.SWEEP_D128 if w.T in (1024, 4096)],
-                         ids=lambda w: w.name)
-def test_d128_sweep_short(w):
+@pytest.mark.parametrize("w", [w for w in syn.SWEEP_D128 if w.T <= 8192], ids=lambda w: w.name)
+def test_d128_sweep_every_element(w):
+    """The d=128 sweep up to T=8K, causal and not: every element of a few
+    seeded (b, h) heads (heads are independent problems, so a subset is
+    exact)."""
     x = syn.make_inputs(w)
     g = gc.run_gpu(x, w)
-    pick = np.random.default_rng(0).choice(w.B * w.H, size=4, replace=False)
+    n_pick = 4 if w.T <= 4096 else (3 if w.causal else 2)
+    pick = np.random.default_rng(w.T).choice(w.B * w.H, size=n_pick, replace=False)
     gc.assert_within(gc.compare_full(x, w, g, pick=pick), w.name)
 
 
-@pytest.mark.parametrize("w", [w for w in syn.SWEEP_D128 if w.T == 32768], ids=lambda w: w.name)
-def test_d128_32k(w):
+# (b, h) problems whose query rows (O, LSE, dQ) and key rows (dK, dV) are
+# checked one by one at the long lengths; the 32K causal workload is the
+# benchmark's, run in the benchmark's launch configuration.
+LONG_HEADS = {
+    "d128_T16K_causal": ([0, 9, 31], [4, 27]),
+    "d128_T16K_noncausal": ([1, 14, 30], [6, 25]),
+    "d128_T32K_causal": ([0, 7, 15], [2, 5, 13]),
+    "d128_T32K_noncausal": ([0, 7, 15], [5, 11]),
+}
+
+
+@pytest.mark.parametrize("w", [w for w in syn.SWEEP_D128 if w.T >= 16384], ids=lambda w: w.name)
+def test_d128_long(w):
     x = syn.make_inputs(w)
     g = gc.run_gpu(x, w)
-    err = gc.compare_sampled(x, w, g, heads=[0, 7, 15], kv_heads=[5] if w.causal else [])
+    heads, kv_heads = LONG_HEADS[w.name]
+    err = gc.compare_sampled(x, w, g, heads=heads, kv_heads=kv_heads)
+    assert {"dK", "dV", "dQ", "O", "LSE"} <= set(err)
     gc.assert_within(err, w.name)
 
 
@@ -193,8 +210,44 @@ def test_d192(w):
         pick = np.random.default_rng(1).choice(w.B * w.H, size=3, replace=False)
         gc.assert_within(gc.compare_full(x, w, g, pick=pick), w.name)
     else:
-        err = gc.compare_sampled(x, w, g, heads=[1, 9], kv_heads=[3] if w.T <= 8192 else [])
+        kv = [3] if w.T <= 8192 else [3, 12]
+        err = gc.compare_sampled(x, w, g, heads=[1, 9], kv_heads=kv)
+        assert {"dK", "dV"} <= set(err)
         gc.assert_within(err, w.name)
+
+
+INFERENCE = (syn.TINY + [syn.GPT2] + [w for w in syn.SWEEP_D128 if w.T == 32768] + syn.D192)
+
+
+@pytest.mark.parametrize("w", INFERENCE, ids=lambda w: w.name)
+def test_inference_forward_against_oracle(w):
+    """Inference mode (lse = NULL: no statistics written) against the oracle's
+    O: every element on the tiny workload, sampled rows elsewhere; and equal,
+    bit for bit, to the training forward's O."""
+    x = syn.make_inputs(w)
+    dev = "cuda:0"
+    if w.layout == syn.LAYOUT_PACKED:
+        qkv = x["qkv"].to(dev)
+        q, k, v = qkv.select(-3, 0), qkv.select(-3, 1), qkv.select(-3, 2)
+    else:
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o_inf, none = binding.forward(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout,
+                                  with_lse=False)
+    o_train, _ = binding.forward(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout)
+    torch.cuda.synchronize()
+    assert binding.attn_fwd_status() == 0
+    assert none is None and torch.equal(o_inf, o_train)
+    o = o_inf.float().cpu()
+    if w.T <= 128:
+        (qp, kp, vp, _), cu = gc.inputs_as_problems(x, w)
+        O_ref, _, _ = oracle.forward(qp, kp, vp, w.causal, w.scale)
+        got = np.stack(gc.problems(o, w, cu))
+        err = {"O": gc.rel_err(got, O_ref), "O_row": gc.row_err(got, O_ref)}
+    else:
+        nprob = w.B * w.H
+        heads = sorted({0, nprob // 2, nprob - 1})
+        err = gc.compare_forward_sampled(x, w, o, heads)
+    gc.assert_within(err, w.name)
 
 
 def test_varlen_deterministic_workload():
@@ -244,16 +297,6 @@ def test_deterministic_and_fast_agree():
         assert gc.rel_err(a[key].numpy(), b[key].numpy()) <= 2e-3, key
     # dK and dV do not depend on the dQ reduction order
     assert torch.equal(a["dK"], b["dK"]) and torch.equal(a["dV"], b["dV"])
-
-
-def test_inference_mode_matches_training_forward():
-    w = syn.TINY[1]
-    x = syn.make_inputs(w)
-    dev = "cuda:0"
-    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    o1, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
-    o2, none = binding.forward(q, k, v, causal=True, scale=w.scale, with_lse=False)
-    assert none is None and torch.equal(o1, o2)
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
