@@ -37,7 +37,7 @@ EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_status"
             "attn_profile_main_kernel", "attn_profile_aux_kernels", "attn_bwd_noalloc",
             "attn_bwd_noalloc_status", "attn_step_host_scratch_size", "attn_step_host",
             "attn_step_host_status", "attn_fwd_window", "attn_bwd_window", "attn_fwd_ex",
-            "attn_bwd_ex", "attn_debug_cache_stats")
+            "attn_bwd_ex", "attn_debug_cache_stats", "attn_debug_set_bwd_variant")
 BLOCK = 128  # rows per block of a block-sparse mask
 
 _lock = threading.Lock()
@@ -97,6 +97,8 @@ def load():
         lib.attn_profile_main_kernel.restype = I
         lib.attn_profile_aux_kernels.argtypes = [P, P, P, P]
         lib.attn_profile_aux_kernels.restype = I
+        lib.attn_debug_set_bwd_variant.argtypes = [I]
+        lib.attn_debug_set_bwd_variant.restype = I
         lib.attn_debug_cache_stats.argtypes = [P]
         lib.attn_debug_cache_stats.restype = I
         lib.attn_debug_set_wait_bias.argtypes = [I]
@@ -270,6 +272,14 @@ def attn_profile_aux_kernels(pre_start=None, pre_stop=None, convert_start=None,
     conv = lambda e: None if e is None else (e.cuda_event if hasattr(e, "cuda_event") else int(e))
     return load().attn_profile_aux_kernels(conv(pre_start), conv(pre_stop), conv(convert_start),
                                            conv(convert_stop))
+
+
+BWD_AUTO, BWD_ONE_CTA, BWD_CTA_PAIR = 0, 1, 2
+
+
+def attn_debug_set_bwd_variant(variant: int) -> int:
+    """Backward main kernel where both apply: 0 library's choice, 1 one CTA, 2 CTA pairs."""
+    return load().attn_debug_set_bwd_variant(int(variant))
 
 
 def attn_debug_cache_stats() -> dict:

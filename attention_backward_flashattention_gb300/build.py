@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libattn_gb300.so")
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_noalloc.cu", "attn_host.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_pair.cu", "attn_noalloc.cu",
+           "attn_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall"]

@@ -19,6 +19,9 @@ using namespace attn;
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Whether the library's choice for eligible backward calls is the CTA-pair
+// main kernel.
+constexpr bool kPairByDefault = false;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -93,10 +96,14 @@ int order_impl(const int* cu, const int* cuk, int nseq, int* order) {
   return ATTN_OK;
 }
 
+// Kinds of schedule table: forward items, backward items (key tiles), backward
+// items on CTA pairs (pairs of key tiles).
+enum TableKind { kFwdTable = 0, kBwdTable = 1, kBwdPairTable = 2 };
+
 // Variable-length tables: sequences by work; items per sequence are (its
-// 256-row query units (forward) or kv-tiles (backward)) x H; q-tiles numbered
-// sequence by sequence.
-void build_tables(const int* cu, const int* cuk, int nseq, int H, bool forward, VarlenTables* t,
+// 256-row query units (forward), kv-tiles or kv-tile pairs (backward)) x H;
+// q-tiles numbered sequence by sequence.
+void build_tables(const int* cu, const int* cuk, int nseq, int H, int kind, VarlenTables* t,
                   int* n_items, int* n_qtiles) {
   std::memset(t, 0, sizeof(*t));
   for (int b = 0; b <= nseq; ++b) {
@@ -108,7 +115,9 @@ void build_tables(const int* cu, const int* cuk, int nseq, int H, bool forward, 
   for (int k = 0; k < nseq; ++k) {
     t->item_start[k] = acc;
     const int s = t->order[k];
-    acc += (forward ? cdiv(cu[s + 1] - cu[s], kFwdRows) : cdiv(cuk[s + 1] - cuk[s], kTile)) * H;
+    const int lq = cu[s + 1] - cu[s], lk = cuk[s + 1] - cuk[s];
+    acc += (kind == kFwdTable ? cdiv(lq, kFwdRows)
+                              : (kind == kBwdTable ? cdiv(lk, kTile) : cdiv(lk, 2 * kTile))) * H;
   }
   t->item_start[nseq] = acc;
   *n_items = acc;
@@ -154,12 +163,12 @@ class HostCache {
     return true;
   }
 
-  void tables(const int* cu, const int* cuk, int nseq, int H, bool forward, VarlenTables* out,
+  void tables(const int* cu, const int* cuk, int nseq, int H, int kind, VarlenTables* out,
               int* n_items, int* n_qtiles) {
     std::lock_guard<std::mutex> g(mu_);
     TabEntry* victim = &tabs_[0];
     for (TabEntry& e : tabs_) {
-      if (e.used != 0 && e.nseq == nseq && e.H == H && e.forward == forward &&
+      if (e.used != 0 && e.nseq == nseq && e.H == H && e.kind == kind &&
           std::memcmp(e.t.cu, cu, (nseq + 1) * sizeof(int)) == 0 &&
           std::memcmp(e.t.cuk, cuk, (nseq + 1) * sizeof(int)) == 0) {
         e.used = ++clock_;
@@ -171,10 +180,10 @@ class HostCache {
       }
       if (e.used < victim->used) victim = &e;
     }
-    build_tables(cu, cuk, nseq, H, forward, &victim->t, &victim->n_items, &victim->n_qtiles);
+    build_tables(cu, cuk, nseq, H, kind, &victim->t, &victim->n_items, &victim->n_qtiles);
     victim->nseq = nseq;
     victim->H = H;
-    victim->forward = forward;
+    victim->kind = kind;
     victim->used = ++clock_;
     std::memcpy(out, &victim->t, sizeof(VarlenTables));
     *n_items = victim->n_items;
@@ -201,7 +210,7 @@ class HostCache {
   };
   struct TabEntry {
     int nseq = 0, H = 0;
-    bool forward = false;
+    int kind = -1;
     int n_items = 0, n_qtiles = 0;
     VarlenTables t;
     uint64_t used = 0;
@@ -247,7 +256,7 @@ struct WsSizes {
 WsSizes ws_sizes(int n_qtiles, int H, int dqk) {
   WsSizes w;
   w.header = 256;
-  w.sem = round256((size_t)n_qtiles * H * sizeof(int));
+  w.sem = round256((size_t)n_qtiles * H * 2 * sizeof(int));
   w.stat = round256((size_t)n_qtiles * H * kTile * sizeof(float));
   w.acc = round256((size_t)n_qtiles * H * kTile * dqk * sizeof(float));
   w.total = w.header + w.sem + 2 * w.stat + w.acc;
@@ -286,6 +295,10 @@ int set_block_mask(SeqShape* sh, const unsigned char* mask, int mask_batches, in
   sh->blk_bstride = mask_batches == 1 ? 0 : (int64_t)mask_heads * nq * nk;
   return ATTN_OK;
 }
+
+// Which backward main kernel runs when the CTA-pair kernel can (0: the
+// library's choice, 1: one CTA per key tile, 2: CTA pairs).
+std::atomic<int> g_bwd_variant{0};
 
 // Host-side fault injection (tests only): added to every ordered-dQ wait
 // target of deterministic backward calls, so that the wait can never succeed.
@@ -391,7 +404,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if (rc) return rc;
   if (varlen) {
     int n_items = 0, n_qt = 0;
-    hc.tables(cu_seqlens, cuk, B, H, true, &tables, &n_items, &n_qt);
+    hc.tables(cu_seqlens, cuk, B, H, kFwdTable, &tables, &n_items, &n_qt);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
@@ -487,16 +500,29 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   rc = set_block_mask(&L.sh, block_mask, mask_batches, mask_heads, B, H, Tq, Tk, cu_seqlens,
                       cuk);
   if (rc) return rc;
+  const int sms = num_sms_current();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  // The CTA-pair main kernel covers d = 128 without a block mask or a left
+  // window edge (causal, non-causal, right-bounded bands; fixed or variable
+  // length), on at least two SMs.
+  const int variant = g_bwd_variant.load();
+  const bool pair_ok = dqk == 128 && dv == 128 && block_mask == nullptr && window_left < 0 &&
+                       sms >= 2;
+  L.pair = pair_ok && variant != 1 && (variant == 2 || kPairByDefault) ? 1 : 0;
+  if (L.pair && (!hc.map(&L.tm_q64, q, dqk, H, rows_q, dqk, lay.q_row, 64) ||
+                 !hc.map(&L.tm_do64, dO, dv, H, rows_q, dv, lay.o_row, 64)))
+    return ATTN_ERR_CUDA;
   int n_qtiles;
   if (varlen) {
     int n_items = 0;
-    hc.tables(cu_seqlens, cuk, B, H, false, &tables, &n_items, &n_qtiles);
+    hc.tables(cu_seqlens, cuk, B, H, L.pair ? kBwdPairTable : kBwdTable, &tables, &n_items,
+              &n_qtiles);
     L.sh.n_items = n_items;
     L.tables = &tables;
     L.lse_head_stride = Tq;
     L.lse_seq_stride = 0;
   } else {
-    L.sh.n_items = B * H * L.sh.nk_tiles;
+    L.sh.n_items = B * H * (L.pair ? cdiv(L.sh.nk_tiles, 2) : L.sh.nk_tiles);
     n_qtiles = B * L.sh.nq_tiles;
     L.tables = nullptr;
     L.lse_head_stride = Tq;
@@ -533,10 +559,8 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   L.prof_start = static_cast<cudaEvent_t>(g_prof_start.load());
   L.prof_stop = static_cast<cudaEvent_t>(g_prof_stop.load());
   for (int e = 0; e < 4; ++e) L.prof_aux[e] = static_cast<cudaEvent_t>(g_prof_aux[e].load());
-  const int sms = num_sms_current();
-  if (sms <= 0) return ATTN_ERR_CUDA;
   L.num_sms = sms;
-  L.grid = std::min(L.sh.n_items, sms);
+  L.grid = L.pair ? 2 * std::min(L.sh.n_items, sms / 2) : std::min(L.sh.n_items, sms);
   L.stream = static_cast<cudaStream_t>(stream);
   return cuda_err(launch_bwd(L, dqk, dv));
 }
@@ -555,6 +579,12 @@ int attn_profile_aux_kernels(void* pre_start, void* pre_stop, void* convert_star
   const bool all = ev[0] && ev[1] && ev[2] && ev[3];
   if (any && !all) return ATTN_ERR_INVALID_ARG;
   for (int e = 0; e < 4; ++e) g_prof_aux[e].store(ev[e]);
+  return ATTN_OK;
+}
+
+int attn_debug_set_bwd_variant(int variant) {
+  if (variant < 0 || variant > 2) return ATTN_ERR_INVALID_ARG;
+  g_bwd_variant.store(variant);
   return ATTN_OK;
 }
 

@@ -46,6 +46,9 @@
 // built for a block mask (kMask) walk only the ones the mask keeps.  In
 // deterministic mode each dQ tile's contributions arrive in descending kv-tile
 // order: a per-(q-tile, head) word holds 1 + the kv tile that added last.
+// For d = 128 without block masks or left window edges the main kernel can
+// instead run on CTA pairs (attn_bwd_pair.cu); the preprocess and the dQ
+// conversion are the same.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -74,6 +77,9 @@ struct RegSplit {
   static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 176, 176, 208
   static_assert(2 * kCompute + kCtl + kDq <= 4 * kLaunch, "register split");
   static_assert(kCompute % 8 == 0 && kCtl % 8 == 0 && kDq % 8 == 0 && kDq <= 256, "setmaxnreg");
+  // the kernel lowers the P/dS and control warpgroups (setmaxnreg.dec) and
+  // raises the dQ warpgroup (setmaxnreg.inc) from the launch count
+  static_assert(kCompute <= kLaunch && kCtl <= kLaunch && kDq >= kLaunch, "setmaxnreg direction");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(256)
     ws.header[0] = 0;  // status
     ws.header[1] = 0;  // work-item counter
   }
-  for (int64_t i = tid; i < (int64_t)n_qtiles * H; i += nthreads) ws.sem[i] = 0;
+  for (int64_t i = tid; i < (int64_t)n_qtiles * H * 2; i += nthreads) ws.sem[i] = 0;
 
   // D and LSE*log2(e) for every real (token, head) row: DV/8 threads per row,
   // 16 bytes each, consecutive threads along the row (coalesced).
@@ -820,7 +826,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
         float* acc = a.ws.dq_acc + g * (kTile * DQK);
         if (a.deterministic) {
-          int* sem = a.ws.sem + g;
+          int* sem = a.ws.sem + 2 * g;
           if (wt == 0) {
             const int target = kMask ? target_m : wait_target();
             const uint64_t t0 = globaltimer();
@@ -846,7 +852,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           named_bar_sync(1, 128);
           if (wt == 0) {
             __threadfence();
-            st_release_gpu(a.ws.sem + g, it.tile + 1);
+            st_release_gpu(a.ws.sem + 2 * g, it.tile + 1);
           }
         }
       }
@@ -996,17 +1002,22 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
 #endif
     a.ws = L.ws;
     a.sh = L.sh;
-    auto* k = L.sh.blk != nullptr ? attn_bwd_main_kernel<DQK, DV, Tables, true>
-                                  : attn_bwd_main_kernel<DQK, DV, Tables, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.grid);
-    cfg.blockDim = dim3(kMainThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = L.stream;
+    cudaError_t e;
     if (L.prof_start && (e = cudaEventRecord(L.prof_start, L.stream)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, L.tm_do, a, tb);
+    if (L.pair) {
+      e = launch_bwd_pair_main(L);
+    } else {
+      auto* k = L.sh.blk != nullptr ? attn_bwd_main_kernel<DQK, DV, Tables, true>
+                                    : attn_bwd_main_kernel<DQK, DV, Tables, false>;
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(L.grid);
+      cfg.blockDim = dim3(kMainThreads);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.stream = L.stream;
+      e = cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, L.tm_do, a, tb);
+    }
     if (e != cudaSuccess) return e;
     if (L.prof_stop && (e = cudaEventRecord(L.prof_stop, L.stream)) != cudaSuccess) return e;
   }

@@ -30,7 +30,8 @@ struct FwdLaunch {
 // Backward workspace (caller-owned device memory), carved in this order.
 struct BwdWorkspace {
   int* header;      // [0] status, [1] work-item counter
-  int* sem;         // per (q-tile, head): contributions added so far (deterministic mode)
+  int* sem;         // per (q-tile, head, tile half): the key tile (or pair) that added last
+                    // (deterministic mode; the one-CTA kernel uses half 0)
   float* nlse2;     // per (q-tile, head, row): -LSE * log2(e); -inf past the sequence end
   float* ndsum;     // per (q-tile, head, row): -D = -rowsum(dO * O); 0 past the end
   float* dq_acc;    // per (q-tile, head): [dqk/4][128][4] fp32 partial dQ
@@ -38,6 +39,8 @@ struct BwdWorkspace {
 
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // panel maps over (d, H, rows)
+  CUtensorMap tm_q64, tm_do64;          // 64-row boxes of q and dO (CTA-pair kernel)
+  int pair;                             // 1: the main kernel runs on CTA pairs
   const void* o;         // bf16 O, for D
   const void* dout;      // bf16 dO, for D
   const float* lse;      // fp32 LSE from the forward
@@ -66,6 +69,9 @@ struct BwdLaunch {
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdLaunch& L, int dqk, int dv);
 cudaError_t launch_bwd(const BwdLaunch& L, int dqk, int dv);
+// The backward main kernel on CTA pairs (dqk = dv = 128; L.grid even, items = key-tile pairs).
+cudaError_t launch_bwd_pair_main(const BwdLaunch& L);
+int bwd_pair_smem_bytes();
 
 // Device address of the forward kernels' status word on the current device.
 int* fwd_status_ptr();

@@ -480,7 +480,8 @@ def run_ours(args, rank, world):
         tf, secs, cores, desc = oracle_sample(w, args.cpu_rows, x=x)
         cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
-    extra = {"parallelism": f"replicas x{world} (independent heads, no exchange)"}
+    extra = {"parallelism": f"replicas x{world} (independent heads, no exchange)",
+             "bwd_kernel": args.bwd_kernel}
     if w.varlen:
         extra["seqlens"] = list(w.varlen)
     line = {
@@ -736,6 +737,8 @@ def main():
                     help="time the inference-mode forward (lse=NULL) instead of the step")
     ap.add_argument("--block-density", type=float, default=0.0,
                     help="time forward + backward under a random block mask of this density")
+    ap.add_argument("--bwd-kernel", default="auto", choices=("auto", "one-cta", "cta-pair"),
+                    help="backward main kernel where both apply (d=128, no block mask)")
     args = ap.parse_args()
     if args.workload not in syn.ALL:
         ap.error(f"unknown workload {args.workload!r}")
@@ -763,6 +766,7 @@ def main():
             build_mod.build()
         if world > 1:
             torch.distributed.barrier()
+        binding.attn_debug_set_bwd_variant({"auto": 0, "one-cta": 1, "cta-pair": 2}[args.bwd_kernel])
         if args.block_density > 0:
             line = run_block_sparse(args, rank, world)
         elif args.fwd_only:

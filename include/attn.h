@@ -266,6 +266,19 @@ int attn_profile_aux_kernels(void* pre_start, void* pre_stop, void* convert_star
                              void* convert_stop);
 
 /*
+ * Which backward main kernel later calls use where both apply (dqk = dv = 128,
+ * no block mask, no left window edge): 0 = the library's choice, 1 = one CTA
+ * per key tile, 2 = CTA pairs (two key tiles per cluster of two CTAs, tcgen05
+ * pair MMAs, dQ contracted over both tiles before its atomics; "深度学习反向传播
+ * 优化：2-CTA MMA模式与内存访问优化" §2.1-2.2 and §3.1).  Both give results within
+ * the same tolerance; deterministic mode is bit-identical run to run with
+ * either, though not between them (the pair kernel adds dQ per pair of key
+ * tiles).  Returns ATTN_ERR_INVALID_ARG for other values.  Tests and
+ * benchmarks use it to run both kernels.
+ */
+int attn_debug_set_bwd_variant(int variant);
+
+/*
  * Counters of the library's host-side cache (TMA tensor maps and the
  * schedule tables of variable-length batches, reused across calls with the
  * same pointers, shapes and options): out4[0] tensor maps encoded, out4[1]

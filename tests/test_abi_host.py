@@ -104,7 +104,9 @@ def test_workspace_size_formula(lib):
     for (B, H, T, dqk, dv, varlen) in [(1, 16, 32768, 128, 128, 0), (8, 12, 1024, 64, 64, 0),
                                        (2, 3, 200, 192, 128, 0), (40, 16, 32768, 128, 128, 1)]:
         tiles = (-(-T // 128) + B) if varlen else B * -(-T // 128)
-        expect = (256 + r256(tiles * H * 4) + 2 * r256(tiles * H * 128 * 4)
+        # header, two semaphores per (q-tile, head) (one per tile half: the
+        # CTA-pair kernel orders each half on its own), -LSE2 and -D rows, dQ
+        expect = (256 + r256(tiles * H * 2 * 4) + 2 * r256(tiles * H * 128 * 4)
                   + r256(tiles * H * 128 * dqk * 4))
         assert binding.attn_bwd_workspace_size(B, H, T, T, dqk, dv, varlen, 0) == expect
     assert binding.attn_bwd_workspace_size(1, 1, 1, 1, 96, 96) == 0
