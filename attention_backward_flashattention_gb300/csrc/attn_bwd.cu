@@ -72,14 +72,16 @@ constexpr int kMmaWarp = 13;
 template <int DQK>
 struct RegSplit {
   static constexpr uint32_t kLaunch = 128;
-  static constexpr uint32_t kCompute = DQK > 128 ? 96 : (DQK > 64 ? 104 : 112);
-  static constexpr uint32_t kCtl = DQK > 128 ? 112 : (DQK > 64 ? 128 : 112);
-  static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 176, 176, 208
+  static constexpr uint32_t kCompute = DQK > 128 ? 88 : (DQK > 64 ? 104 : 112);
+  // the MMA issuer (control warpgroup) holds every staged descriptor base:
+  // 136 at d <= 128 keeps it from spilling (raised with setmaxnreg.inc)
+  static constexpr uint32_t kCtl = DQK > 128 ? 128 : 136;
+  static constexpr uint32_t kDq = 4 * kLaunch - 2 * kCompute - kCtl;  // 152, 168, 208
   static_assert(2 * kCompute + kCtl + kDq <= 4 * kLaunch, "register split");
   static_assert(kCompute % 8 == 0 && kCtl % 8 == 0 && kDq % 8 == 0 && kDq <= 256, "setmaxnreg");
   // the kernel lowers the P/dS and control warpgroups (setmaxnreg.dec) and
   // raises the dQ warpgroup (setmaxnreg.inc) from the launch count
-  static_assert(kCompute <= kLaunch && kCtl <= kLaunch && kDq >= kLaunch, "setmaxnreg direction");
+  static_assert(kCompute <= kLaunch && kDq >= kLaunch, "setmaxnreg direction");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -419,7 +421,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= 12) {
-   regs_dec<RegSplit<DQK>::kCtl>();
+   if constexpr (RegSplit<DQK>::kCtl > RegSplit<DQK>::kLaunch) regs_inc<RegSplit<DQK>::kCtl>();
+   else regs_dec<RegSplit<DQK>::kCtl>();
    if (warp == kTmaWarp && lane == 0) {
     // ================================================= producer / claimer
     {
@@ -565,8 +568,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           return *static_cast<volatile int*>(&bars->q_last[st]) != 0;
         };
         if (!(ok = W(bars->kv_full, k & 1))) break;
-        // dK/dV accumulators of the previous item read out by the epilogue
-        if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+        if (none || C::kSharedSdP) {
+          // dK/dV accumulators of the previous item read out by the epilogue
+          if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+        }
         if (none) {
           // no query sees this kv tile (a local window or a block mask): the
           // epilogue writes zeros; nothing to compute
@@ -580,6 +585,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (C::kDqOnDp && gi > 0 && !(ok = W(bars->dq_free, (gi - 1) & 1))) break;
           if (!(ok = W(bars->do_full[st0], (q_it / C::kStages) & 1))) break;
           mma_dP(st0);
+          // the previous item's dK/dV accumulators must be read out by its
+          // epilogue before this item's first dV; waiting here, after the first
+          // S and dP, lets the epilogue overlap them
+          if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
           bool go = true;  // kMask: the previous q-tile was not the item's last
           for (int i = i0; kMask ? go : i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;

@@ -104,7 +104,37 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= Cfg::kBarBytes, "barrier block size");
 
+// Optional phase trace of the first cluster (compiled in only with
+// -DATTN_TRACE): the first thread of each role stores (clock64 << 8 | event)
+// for q-tile steps [ATTN_TRACE_FROM, ATTN_TRACE_FROM + 8), 64 records per
+// thread, indexed by (CTA, thread).  Clocks are per SM: compare events of one
+// CTA only.
+#ifdef ATTN_TRACE
+#ifndef ATTN_TRACE_FROM
+#define ATTN_TRACE_FROM 40
+#endif
+constexpr int kTraceCap = 64;
+#define PAIR_TRACE_DECL int tr_n = 0
+#define PAIR_TRACE(ev, step)                                                                 \
+  do {                                                                                       \
+    if (a.trace != nullptr && blockIdx.x < 2 && (uint32_t)(step) >= ATTN_TRACE_FROM &&      \
+        (uint32_t)(step) < ATTN_TRACE_FROM + 8 && tr_n < kTraceCap)                          \
+      a.trace[(blockIdx.x * kThreads + threadIdx.x) * kTraceCap + tr_n++] =                  \
+          ((unsigned long long)clock64() << 8) | (unsigned)(ev);                             \
+  } while (0)
+#else
+#define PAIR_TRACE_DECL \
+  do {                  \
+  } while (0)
+#define PAIR_TRACE(ev, step) \
+  do {                       \
+  } while (0)
+#endif
+
 struct PairArgs {
+#ifdef ATTN_TRACE
+  unsigned long long* trace;
+#endif
   int sem_bias;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -196,6 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const SeqShape& sh = a.sh;
   Abort ab{&bars->abort_flag, a.ws.header};
+  PAIR_TRACE_DECL;
   const bool misaligned = (smem_u32(smem) & 1023u) != 0;
   if (threadIdx.x == 0) {
     bars->abort_flag = misaligned ? 1 : 0;
@@ -298,10 +329,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // in the order the MMAs free the slots: dV (dO halves), S (Q rows),
           // dK (Q halves), dP (dO rows)
           if (!(ok = mbar_wait(smem_u32(&bars->dov_empty[st]), par2 ^ 1, ab))) break;
+          PAIR_TRACE(50, u);
           if (leader) mbar_arrive_expect_tx(smem_u32(&bars->dov_full[st]), C::kSlotTx);
           tma_load_3d_pair(sdOv + st * kPanel, &tm_do, L(bars->dov_full[st]), (int)rank * 64,
                            it.head, qrow);
           if (!(ok = mbar_wait(smem_u32(&bars->qs_empty), par1 ^ 1, ab))) break;
+          PAIR_TRACE(51, u);
           if (leader) mbar_arrive_expect_tx(smem_u32(&bars->qs_full), C::kHalfTx);
           for (int p = 0; p < 2; ++p)
             tma_load_3d_pair(sQs + p * kHalfPanel, &tm_q64, L(bars->qs_full), p * 64, it.head,
@@ -314,10 +347,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.ndsum + g * kTile, kTile * 4, sb);
           }
           if (!(ok = mbar_wait(smem_u32(&bars->qk_empty[st]), par2 ^ 1, ab))) break;
+          PAIR_TRACE(53, u);
           if (leader) mbar_arrive_expect_tx(smem_u32(&bars->qk_full[st]), C::kSlotTx);
           tma_load_3d_pair(sQk + st * kPanel, &tm_q, L(bars->qk_full[st]), (int)rank * 64,
                            it.head, qrow);
           if (!(ok = mbar_wait(smem_u32(&bars->dop_empty), par1 ^ 1, ab))) break;
+          PAIR_TRACE(54, u);
           if (leader) mbar_arrive_expect_tx(smem_u32(&bars->dop_full), C::kHalfTx);
           for (int p = 0; p < 2; ++p)
             tma_load_3d_pair(sdOp + p * kHalfPanel, &tm_do64, L(bars->dop_full), p * 64, it.head,
@@ -420,22 +455,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t st = q_it & 1, par2 = (q_it >> 1) & 1;
             const bool first = i == i0, more = i + 1 < i1;
             if (!(ok = W(bars->p_full, gi & 1))) break;
+            PAIR_TRACE(10, gi);
             if (!(ok = W(bars->dov_full[st], par2))) break;
+            PAIR_TRACE(11, gi);
             mma_dV(st, first);
             if (more) {
               if (!(ok = W(bars->qs_full, (q_it + 1) & 1))) break;
+              PAIR_TRACE(12, gi);
               mma_S();
             }
             if (!(ok = W(bars->ds_half[0], gi & 1))) break;
+            PAIR_TRACE(13, gi);
             if (!(ok = W(bars->qk_full[st], par2))) break;
+            PAIR_TRACE(14, gi);
             mma_dK(st, first, 0);
             if (!(ok = W(bars->ds_half[1], gi & 1))) break;
+            PAIR_TRACE(15, gi);
             mma_dK(st, first, 1);
             commit(bars->qk_empty[st]);
             mma_dQ();  // after dK: dQ's columns hold half of dS^T until dK has read it
+            PAIR_TRACE(16, gi);
             if (more) {
               if (!(ok = W(bars->dq_free, gi & 1))) break;
+              PAIR_TRACE(17, gi);
               if (!(ok = W(bars->dop_full, (q_it + 1) & 1))) break;
+              PAIR_TRACE(18, gi);
               mma_dP();
             }
           }
@@ -481,6 +525,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float* ndsum = nlse2 + kTile;
         if (!(ok = mbar_wait_warp(smem_u32(&bars->s_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && (warp & 3) == 0) PAIR_TRACE(20, gi);
         uint32_t pk[32];
         const int qrel = kidx0 - kTile * i - grp * 64;
         const int qmin = !key_ok ? 64 : (sh.wr >= 0 ? min(64, max(0, qrel - band_off(sh, it) - sh.wr)) : 0);
@@ -525,11 +570,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(L(bars->p_full));
+        if (lane == 0 && (warp & 3) == 0) PAIR_TRACE(21, gi);
         // ---- dS^T = P^T ⊙ (dP^T − D): bf16 into TMEM (dK) and into the dQ operand
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dp_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && (warp & 3) == 0) PAIR_TRACE(22, gi);
         // the previous step's dK and dQ products are done with both copies
         if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->ds_free), (gi - 1) & 1, ab))) break;
+        if (lane == 0 && (warp & 3) == 0) PAIR_TRACE(23, gi);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dr[32];
@@ -560,6 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(L(bars->ds_half[c]));
+          if (lane == 0 && (warp & 3) == 0) PAIR_TRACE(24 + c, gi);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->stat_empty[st]));
@@ -589,6 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = i0; i < i1; ++i, ++gi) {
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
+        if (lane == 0 && warp == 8) PAIR_TRACE(30, gi);
         uint32_t qv[64];
         tmem_ld32(tmem + lane_base + C::kTmemdQ, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
         tmem_ld32(tmem + lane_base + C::kTmemdQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
@@ -596,6 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(L(bars->dq_free));
+        if (lane == 0 && warp == 8) PAIR_TRACE(31, gi);
         const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
         float* acc = a.ws.dq_acc + g * (kTile * 128);
         if (a.deterministic) {
@@ -622,6 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           red_add_v4(acc + ((dh * 16 + c4) * kTile + qr) * 4, __uint_as_float(qv[c4 * 4 + 0]),
                      __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
                      __uint_as_float(qv[c4 * 4 + 3]));
+        if (lane == 0 && warp == 8) PAIR_TRACE(32, gi);
         if (a.deterministic) {
           named_bar_sync(1, 128);
           if (wt == 0) {
@@ -703,8 +755,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 int bwd_pair_smem_bytes() { return Cfg::kSmemBytes; }
 
+#ifdef ATTN_TRACE
+unsigned long long* g_pair_trace = nullptr;
+#endif
+
 cudaError_t launch_bwd_pair_main(const BwdLaunch& L) {
   PairArgs a;
+#ifdef ATTN_TRACE
+  a.trace = g_pair_trace;
+#endif
   a.sem_bias = L.sem_bias;
   a.dk = reinterpret_cast<__nv_bfloat16*>(L.dk);
   a.dv = reinterpret_cast<__nv_bfloat16*>(L.dv);
@@ -738,3 +797,10 @@ cudaError_t launch_bwd_pair_main(const BwdLaunch& L) {
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Trace builds only: buffer of 2 x 512 x 64 records for the first cluster (null = off).
+extern "C" void attn_pair_trace_set(void* buf) {
+  attn::g_pair_trace = static_cast<unsigned long long*>(buf);
+}
+#endif
