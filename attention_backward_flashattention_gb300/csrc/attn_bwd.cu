@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           return *static_cast<volatile int*>(&bars->q_last[st]) != 0;
         };
         if (!(ok = W(bars->kv_full, k & 1))) break;
-        if (none || C::kSharedSdP) {
+        if (none) {
           // dK/dV accumulators of the previous item read out by the epilogue
           if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
         }
@@ -640,6 +640,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mma_S(st);
             if (!(ok = W(bars->p_full, gi & 1))) break;
             if (!(ok = W(bars->do_full[st], par))) break;
+            // the previous item's dK/dV accumulators read out by its epilogue,
+            // which overlaps this item's first S and P
+            if (first && !(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
             mma_dV(st, first);
             mma_dP(st);  // overwrites the S/P columns after dV has read P
             mma_commit(smem_u32(&bars->do_empty[st]));
