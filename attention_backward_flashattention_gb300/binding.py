@@ -333,6 +333,14 @@ def attn_varlen_order(cu_seqlens) -> list:
 # Conveniences: shapes from tensors, outputs allocated with torch
 # ----------------------------------------------------------------------------
 def _dims(q, k, v, cu_seqlens, layout):
+    # the library sees only pointers: a tensor whose rank does not match the
+    # layout would be read with the wrong sizes
+    rank = (3 if cu_seqlens is not None else 4) + (1 if layout == LAYOUT_PACKED_QKV else 0)
+    if layout == LAYOUT_PACKED_QKV:
+        rank -= 1  # q, k, v are slot views: (..., H, d) of a (..., 3, H, d) buffer
+    if any(t.dim() != rank for t in (q, k, v)):
+        raise ValueError(f"q, k, v must have {rank} dimensions for this layout "
+                         f"({'variable length' if cu_seqlens is not None else 'fixed length'})")
     if layout == LAYOUT_PACKED_QKV:
         # q, k, v are slot views of one (..., 3, H, d) buffer
         H, dqk = q.shape[-2], q.shape[-1]

@@ -938,7 +938,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// 3. dQ conversion: one CTA per (q-tile, head)
+// 3. dQ conversion: one CTA per half (64 rows) of a (q-tile, head)
 // ---------------------------------------------------------------------------
 template <int DQK, typename Tables>
 __global__ void __launch_bounds__(256)
@@ -946,23 +946,25 @@ __global__ void __launch_bounds__(256)
                             const int64_t dq_row_stride, const float scale, const SeqShape sh,
                             const __grid_constant__ Tables tb) {
   using S = SeqOf<Tables>;
-  extern __shared__ float tile_s[];  // [128][DQK + 4]
+  extern __shared__ float tile_s[];  // [64][DQK + 4]
   constexpr int kLd = DQK + 4;
-  const int g = blockIdx.x / sh.H;
-  const int h = blockIdx.x - g * sh.H;
+  constexpr int kR = 64;
+  const int th = blockIdx.x >> 1, hf = blockIdx.x & 1;
+  const int g = th / sh.H;
+  const int h = th - g * sh.H;
   int s, i;
   S::tile_of(sh, tb, g, s, i);
   const int L = S::length(sh, tb, s);
-  const int rows = min(kTile, L - i * kTile);
-  const float4* src = reinterpret_cast<const float4*>(dq_acc + (int64_t)blockIdx.x * kTile * DQK);
-  for (int idx = threadIdx.x; idx < kTile * DQK / 4; idx += blockDim.x) {
-    const int c4 = idx / kTile, r = idx - c4 * kTile;
-    const float4 v = src[idx];
+  const int rows = max(0, min(kR, L - i * kTile - hf * kR));
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (int64_t)th * kTile * DQK);
+  for (int idx = threadIdx.x; idx < kR * DQK / 4; idx += blockDim.x) {
+    const int c4 = idx / kR, r = idx - c4 * kR;
+    const float4 v = src[c4 * kTile + hf * kR + r];
     float* d = tile_s + r * kLd + c4 * 4;
     d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
   }
   __syncthreads();
-  const int64_t row0 = S::row0(sh, tb, s) + (int64_t)i * kTile;
+  const int64_t row0 = S::row0(sh, tb, s) + (int64_t)i * kTile + hf * kR;
   for (int idx = threadIdx.x; idx < rows * (DQK / 8); idx += blockDim.x) {
     const int r = idx / (DQK / 8), c8 = idx - r * (DQK / 8);
     const float* f = tile_s + r * kLd + c8 * 8;
@@ -986,7 +988,9 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
   // 1. preprocess
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.num_sms * 4);
+    // many small blocks: each thread has one O / dO pair in flight per loop
+    // step, so occupancy carries the bandwidth (32 blocks per SM measured best)
+    cfg.gridDim = dim3(L.num_sms * 32);
     cfg.blockDim = dim3(256);
     cfg.stream = L.stream;
     cudaError_t e;
@@ -1035,12 +1039,12 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
   }
   // 3. dQ conversion
   {
-    const int smem = kTile * (DQK + 4) * 4;
+    const int smem = 64 * (DQK + 4) * 4;
     auto* k = attn_bwd_convert_kernel<DQK, Tables>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.n_qtiles * L.sh.H);
+    cfg.gridDim = dim3(L.n_qtiles * L.sh.H * 2);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
