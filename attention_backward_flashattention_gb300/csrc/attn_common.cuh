@@ -15,10 +15,14 @@
 // §3.2 "确定性执行实现": CTA order swizzled over heads/batches for L2 reuse,
 // longest-processing-time-first over batches, and shortest-first over causal
 // kv-tiles for the deterministic dQ reduction):
-//   forward   item = (sequence, head, 256-row unit m: two q-tiles), taken by a
-//             static round-robin over CTAs: units with the longest causal row
-//             range first (m descending), heads varying fastest, which keeps
-//             the round-robin balanced.
+//   forward   item = (sequence, head, 256-row unit m: two q-tiles), claimed
+//             dynamically (a per-call counter): all units of one (sequence,
+//             head) are consecutive, the longest causal row range first (m
+//             descending), so one head's K and V stay in L2 while ~one SM count
+//             of its units run, and the last items claimed are the shortest.
+//             When every head's K and V fit in L2 together (fixed length), the
+//             units go rank-major instead (longest of every head first), which
+//             balances better when each CTA gets only a few items.
 //   backward  item = (sequence, head, kv-tile n); all tiles of one (sequence,
 //             head) are consecutive, so one head's Q, dO and fp32 dQ
 //             accumulator stay in L2 while ~one SM count of its kv-tiles run.
@@ -66,6 +70,7 @@ struct SeqShape {
   int band_off;
   int wl, wr;
   int descending;  // backward only: 1 = kv-tiles n descending (deterministic mode)
+  int rank_major;  // forward, fixed length: 1 = units rank-major ((b, h) fastest)
   // Block mask (null: every tile pair in the band takes part).  Byte
   // [b][h][qt][kt] of a (mask batches, mask heads, q-tiles, kv-tiles) array;
   // a zero byte drops the pair (query tile qt, key tile kt) of sequence b,
@@ -90,18 +95,22 @@ template <typename Tables>
 __device__ __forceinline__ Item decode_item(const SeqShape& sh, const Tables& tb, int item,
                                             bool forward);
 
-// Fixed length.  Forward: item / (B*H) is the q-tile's rank (longest first) and
-// the remainder the (b, h), so a static round-robin over CTAs stays balanced.
-// Backward (claimed dynamically): item / (kv-tiles per head) is the (b, h).
+// Fixed length (items claimed dynamically): item / (units or kv-tiles per head)
+// is the (b, h), the remainder the unit's or tile's rank.
 template <>
 __device__ __forceinline__ Item decode_item<NoTables>(const SeqShape& sh, const NoTables&,
                                                       int item, bool forward) {
   Item it;
   int bh, rank;
-  if (forward) {  // unit rank major, (b, h) fastest; it.tile = 256-row unit
-    const int nbh = sh.nseq * sh.H;
-    rank = item / nbh;
-    bh = item - rank * nbh;
+  if (forward) {  // 256-row units longest first; it.tile = unit
+    if (sh.rank_major) {  // unit rank major, (b, h) fastest
+      const int nbh = sh.nseq * sh.H;
+      rank = item / nbh;
+      bh = item - rank * nbh;
+    } else {              // (b, h) major
+      bh = item / sh.nq_units;
+      rank = item - bh * sh.nq_units;
+    }
     it.tile = sh.nq_units - 1 - rank;
   } else {        // (b, h) major, tile rank fastest
     bh = item / sh.nk_tiles;
@@ -139,14 +148,9 @@ __device__ __forceinline__ Item decode_item<VarlenTables>(const SeqShape& sh,
   it.band_off = it.Lk - it.Lq;
   // forward items: 256-row query units; backward items: kv-tiles
   const int nt = forward ? cdiv(it.Lq, kFwdRows) : cdiv(it.Lk, kTile);
-  int rank;
-  if (forward) {  // tile rank, then head
-    rank = local / sh.H;
-    it.head = local - rank * sh.H;
-  } else {        // head, then tile rank
-    it.head = local / nt;
-    rank = local - it.head * nt;
-  }
+  // head, then tile rank
+  it.head = local / nt;
+  const int rank = local - it.head * nt;
   if (forward) it.tile = nt - 1 - rank;
   else it.tile = sh.descending ? nt - 1 - rank : rank;
   it.tile_base = tb.tile_start[it.seq];

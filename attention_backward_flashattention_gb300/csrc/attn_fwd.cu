@@ -10,12 +10,14 @@
 // division by the row sum happens once, after the loop).
 //
 // One CTA (384 threads) per SM, persistent over work items; an item is two
-// consecutive 128-row Q tiles of one (sequence, head) (see attn_common.cuh for
-// the order):
+// consecutive 128-row Q tiles of one (sequence, head).  The producer claims
+// items from a per-call counter (head-major, longest first within a head; see
+// attn_common.cuh) and hands each to the other roles through a 2-slot ring, so
+// the CTAs running at any moment share a few heads' K and V in L2:
 //   warps 0-3, 4-7  softmax warpgroup w owns Q tile w: thread r holds query
 //                   row r (TMEM lane r)
-//   warp 8          TMA producer: the two Q tiles once per item, K and V tiles
-//                   into rings of their own
+//   warp 8          TMA producer and work claimer: the two Q tiles once per
+//                   item, K and V tiles into rings of their own
 //   warp 9          MMA issuer: S_w = Q_w K^T and O_w += P_w V
 // Tensor memory: S_0, S_1 at columns [0,128), [128,256), O_0, O_1 after them.
 // P is written back into the S columns as bf16 pairs and read from there by
@@ -106,12 +108,14 @@ struct FwdCfg {
 };
 
 struct FwdBars {
+  uint64_t item_full[2], item_empty[2];  // work items handed from the producer to the other roles
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int item_slot[2];
   // block mask only, written by the producer before the matching arrive:
   int q_none;       // 1: the item loads no kv tile (with q_full)
   int kv_flags[4];  // per K stage (with k_full): kKvUse0 | kKvUse1 | kKvFirst0 | ...
@@ -201,14 +205,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, const int64_t o_row_stride,
                     const int64_t lse_head_stride, const int64_t lse_seq_stride,
-                    const float scale_log2, int* status, const SeqShape sh_in,
+                    const float scale_log2, int* status, int* claim, const SeqShape sh_in,
                     const __grid_constant__ Tables tb) {
   using C = FwdCfg<DQK, DV>;
   SeqShape sh = sh_in;
   if constexpr (!kLeft) sh.wl = -1;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // Every CTA counts out on claim[1] once it will claim no more items; the
+  // last one leaves both counters at zero for the next call that uses them.
+  auto count_out = [&]() {
+    __threadfence();  // this CTA's claims are ordered before its count-out
+    if (atomicAdd(&claim[1], 1) == (int)gridDim.x - 1) {
+      atomicExch(&claim[0], 0);
+      atomicExch(&claim[1], 0);
+    }
+  };
   if (smem_u32(smem) & 1023u) {  // the swizzled panels need a 1024-byte aligned window
-    if (threadIdx.x == 0) atomicCAS(status, 0, kStatusInternal);
+    if (threadIdx.x == 0) {
+      atomicCAS(status, 0, kStatusInternal);
+      count_out();
+    }
     return;
   }
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kOffBar);
@@ -221,6 +237,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (threadIdx.x == 0) {
     bars->abort_flag = 0;
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&bars->item_full[k]), 1);
+      mbar_init(smem_u32(&bars->item_empty[k]), 1 + 8);  // MMA thread + softmax warps
+    }
     mbar_init(smem_u32(&bars->q_full), 1);
     mbar_init(smem_u32(&bars->q_empty), 1);
     for (int s = 0; s < C::kKStages; ++s) {
@@ -260,7 +280,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     {
       uint32_t kv_it = 0, item_iter = 0, q_issued = 0, k_issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
+      // claim the next work item (items are taken in order by all CTAs) and
+      // hand it to the MMA issuer and the softmax warps through a 2-slot ring
+      auto claim_next = [&]() -> int {
+        const uint32_t slot = item_iter & 1;
+        if (!mbar_wait(smem_u32(&bars->item_empty[slot]), ((item_iter >> 1) & 1) ^ 1, ab)) {
+          ok = false;
+          return sh.n_items;
+        }
+        const int item = atomicAdd(claim, 1);
+        bars->item_slot[slot] = item;
+        mbar_arrive(smem_u32(&bars->item_full[slot]));
+        return item;
+      };
+      for (int item = claim_next(); ok && item < sh.n_items; ++item_iter, item = claim_next()) {
         const Item it = decode_item(sh, tb, item, true);
         int lo0, hi0, lo1, hi1;
         kv_ranges(sh, it, lo0, hi0, lo1, hi1);
@@ -326,6 +359,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++kv_it;
         }
       }
+      count_out();
       if (!ok) {
         // let every copy already issued land before the CTA's memory is released
         for (uint32_t t = k_issued > (uint32_t)C::kKStages ? k_issued - C::kKStages : 0;
@@ -387,7 +421,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         return true;
       };
       auto flag = [&](const int& v) { return *static_cast<const volatile int*>(&v); };
-      for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x, ++item_iter) {
+      auto read_next = [&]() -> int {
+        const uint32_t slot = item_iter & 1;
+        if (!mbar_wait(smem_u32(&bars->item_full[slot]), (item_iter >> 1) & 1, ab)) {
+          ok = false;
+          return sh.n_items;
+        }
+        const int item = *static_cast<volatile int*>(&bars->item_slot[slot]);
+        mbar_arrive(smem_u32(&bars->item_empty[slot]));
+        return item;
+      };
+      for (int item = read_next(); ok && item < sh.n_items; ++item_iter, item = read_next()) {
         const Item it = decode_item(sh, tb, item, true);
         int lo0, hi0, lo1, hi1;
         kv_ranges(sh, it, lo0, hi0, lo1, hi1);
@@ -484,9 +528,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::kTmemS + w * 128;
     const uint32_t tO = tmem + lane_base + C::kTmemO + w * DV;
-    uint32_t cnt = 0, items_done = 0;
+    uint32_t cnt = 0, items_done = 0, n_read = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < sh.n_items; item += gridDim.x) {
+    auto read_next = [&]() -> int {
+      const uint32_t slot = n_read & 1;
+      if (!mbar_wait_warp(smem_u32(&bars->item_full[slot]), (n_read >> 1) & 1, ab)) {
+        ok = false;
+        return sh.n_items;
+      }
+      const int item = *static_cast<volatile int*>(&bars->item_slot[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->item_empty[slot]));
+      ++n_read;
+      return item;
+    };
+    for (int item = read_next(); ok && item < sh.n_items; item = read_next()) {
       const Item it = decode_item(sh, tb, item, true);
       int lo0, hi0, lo1, hi1;
       kv_ranges(sh, it, lo0, hi0, lo1, hi1);
@@ -668,15 +724,15 @@ cudaError_t launch_kernel(const FwdLaunch& L) {
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v,
                               reinterpret_cast<__nv_bfloat16*>(L.o), L.lse, L.o_row_stride,
-                              L.lse_head_stride, L.lse_seq_stride, L.scale_log2, L.status, L.sh,
-                              *L.tables);
+                              L.lse_head_stride, L.lse_seq_stride, L.scale_log2, L.status, L.claim,
+                              L.sh, *L.tables);
   }
   auto* k = attn_fwd_kernel<DQK, DV, NoTables, kMask, kLeft>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, reinterpret_cast<__nv_bfloat16*>(L.o),
                             L.lse, L.o_row_stride, L.lse_head_stride, L.lse_seq_stride,
-                            L.scale_log2, L.status, L.sh, NoTables{});
+                            L.scale_log2, L.status, L.claim, L.sh, NoTables{});
 }
 
 template <int DQK, int DV>
@@ -691,6 +747,18 @@ cudaError_t launch_typed(const FwdLaunch& L) {
 // Sticky status word of the forward kernels on each device (a bounded wait
 // that gave up writes its code here; attn_fwd_status reads and clears it).
 __device__ int g_fwd_status = 0;
+
+// Work-item counters of the forward: a pair (items claimed, CTAs done) per
+// call in flight, taken round-robin, so up to kFwdClaimSlots calls may
+// overlap on different streams.  A kernel leaves its pair at zero.
+__device__ int g_fwd_claim[2 * kFwdClaimSlots];
+
+int* fwd_claim_ptr(int slot) {
+  void* p = nullptr;
+  if (slot < 0 || slot >= kFwdClaimSlots) return nullptr;
+  if (cudaGetSymbolAddress(&p, g_fwd_claim) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p) + 2 * slot;
+}
 
 int* fwd_status_ptr() {
   void* p = nullptr;

@@ -21,6 +21,7 @@ struct FwdLaunch {
   int64_t lse_seq_stride;        // fixed length: elements between sequences; varlen: 0
   float scale_log2;              // scale * log2(e)
   int* status;                   // device status word
+  int* claim;                    // device counters (items claimed, CTAs done), zero at launch
   SeqShape sh;
   const VarlenTables* tables;    // null for fixed-length batches
   int grid;
@@ -75,6 +76,9 @@ int bwd_pair_smem_bytes();
 
 // Device address of the forward kernels' status word on the current device.
 int* fwd_status_ptr();
+// Device address of forward work-item counter `slot` on the current device.
+constexpr int kFwdClaimSlots = 256;
+int* fwd_claim_ptr(int slot);
 
 // Dynamic shared memory the kernels need (for validation / tests).
 int fwd_smem_bytes(int dqk, int dv);
