@@ -34,8 +34,9 @@
 //   warps 0-3, 4-7  P / dS warpgroups; thread = key row (TMEM lane); group g
 //                   handles query columns [64g, 64g+64) of S^T and dP^T
 //   warps 8-11      dQ warpgroup: drains dQ_i from TMEM (thread = query row) and
-//                   adds it to the fp32 accumulator (ordered in deterministic
-//                   mode); at the end of an item stores dK and dV
+//                   adds it to the fp32 accumulator (spread over the q-tile
+//                   step in fast mode, ordered in deterministic mode); at the
+//                   end of an item stores dK and dV
 //   warp 12         TMA producer and work-item claimer
 //   warp 13         MMA issuer, tensor-memory owner (warps 14-15 idle)
 // MMA order per q-tile: ... dV_i, S_{i+1}, dK_i (first half), dQ_i, dK_i
@@ -85,28 +86,64 @@ struct RegSplit {
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Optional phase tracing of CTA 0 (compiled in only with -DATTN_TRACE): each
-// recording thread stores (clock64 << 8 | event) for q-tile steps
-// [kTraceFrom, kTraceFrom + 8) straight to the caller's buffer (64 records per
-// thread, indexed by thread; the caller zeroes it).
+// Optional phase tracing of CTA 0 (compiled in only with -DATTN_TRACE): the
+// recording threads keep the low 32 bits of clock64 per (event, step) for the
+// q-tile steps [kTraceFrom, kTraceFrom + kTraceSteps) in 512 bytes of shared
+// memory past the kernel's own, and the CTA copies the 128 words to the
+// caller's buffer (as 64-bit values) at exit.  Keeping the records on chip
+// matters: a global store per event would queue behind the dQ reductions and
+// delay the recording thread itself.
 #ifdef ATTN_TRACE
-constexpr int kTraceCap = 64;
 #ifndef ATTN_TRACE_FROM
 #define ATTN_TRACE_FROM 40
 #endif
 constexpr uint32_t kTraceFrom = ATTN_TRACE_FROM;
-#define ATTN_TRACE_DECL int tr_n = 0
-#define ATTN_TRACE_EV(ev, step)                                                              \
-  do {                                                                                       \
-    if (a.trace != nullptr && blockIdx.x == 0 && (step) >= kTraceFrom &&                     \
-        (step) < kTraceFrom + 8 && tr_n < kTraceCap)                                         \
-      a.trace[threadIdx.x * kTraceCap + tr_n++] =                                            \
-          ((unsigned long long)clock64() << 8) | (unsigned)(ev);                             \
+constexpr uint32_t kTraceSteps = 4;
+constexpr int kTraceSmem = 512;
+// record slot of an event: MMA issuer 0-6, P/dS warpgroup 0 7-12, group 1
+// 13-18, dQ warpgroup 19-21, producer 22-25, load observers 26-27
+__device__ __forceinline__ int trace_index(int ev, int warp) {
+  switch (ev) {
+    case 10: return 0;
+    case 11: return 1;
+    case 12: return 2;
+    case 15: return 3;
+    case 16: return 4;
+    case 13: return 5;
+    case 14: return 6;
+    case 20: case 21: case 22: case 25: case 23: case 24: {
+      const int b = ev == 20 ? 0 : ev == 21 ? 1 : ev == 22 ? 2 : ev == 25 ? 3 : ev == 23 ? 4 : 5;
+      return 7 + (warp >= 4 ? 6 : 0) + b;
+    }
+    case 30: return 19;
+    case 31: return 20;
+    case 32: return 21;
+    case 41: return 22;
+    case 42: return 23;
+    case 40: return 24;
+    case 43: return 25;
+    case 44: return 26;
+    case 45: return 27;
+    default: return -1;
+  }
+}
+#define ATTN_TRACE_DECL uint32_t* const tr_smem = reinterpret_cast<uint32_t*>(smem + C::kSmemBytes)
+#define ATTN_TRACE_EV(ev, step)                                                             \
+  do {                                                                                      \
+    const uint32_t s_ = (uint32_t)(step) - kTraceFrom;                                      \
+    if (a.trace != nullptr && blockIdx.x == 0 && s_ < kTraceSteps) {                        \
+      const int ix_ = trace_index(ev, warp);                                                \
+      if (ix_ >= 0) tr_smem[ix_ * kTraceSteps + s_] = (uint32_t)clock64();                  \
+    }                                                                                       \
   } while (0)
-#define ATTN_TRACE_FLUSH \
-  do {                   \
+#define ATTN_TRACE_FLUSH                                                                    \
+  do {                                                                                      \
+    __syncthreads();                                                                        \
+    if (a.trace != nullptr && blockIdx.x == 0 && threadIdx.x < kTraceSmem / 4)              \
+      a.trace[threadIdx.x] = tr_smem[threadIdx.x];                                          \
   } while (0)
 #else
+constexpr int kTraceSmem = 0;
 #define ATTN_TRACE_DECL \
   do {                  \
   } while (0)
@@ -359,6 +396,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                          const __grid_constant__ CUtensorMap tm_do, const MainArgs a,
                          const __grid_constant__ Tables tb) {
   using C = BwdCfg<DQK, DV>;
+  static_assert(C::kSmemBytes + kTraceSmem <= kMaxSmem, "shared memory budget (trace)");
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled panels need a 1024-byte aligned window
     if (threadIdx.x == 0) atomicCAS(a.ws.header, 0, kStatusInternal);
@@ -380,6 +418,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   auto sdO_of = [&](uint32_t st) { return sStage + st * (C::kQBytes + C::kdOBytes) + C::kQBytes; };
 
   if (threadIdx.x == 0) {
+#ifdef ATTN_TRACE
+    for (int t = 0; t < kTraceSmem / 4; ++t) tr_smem[t] = 0;
+#endif
     bars->abort_flag = 0;
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&bars->item_full[k]), 1);
@@ -426,7 +467,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
    if (warp == kTmaWarp && lane == 0) {
     // ================================================= producer / claimer
     {
-      uint32_t q_it = 0, kq = 0, q_issued = 0;
+      uint32_t q_it = 0, kq = 0, q_issued = 0, do_issued = 0;
       bool ok = true, kv_issued = false;
       for (uint32_t k = 0;; ++k) {
         const uint32_t slot = k & 1;
@@ -471,12 +512,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           bulk_load(sStat + st * C::kStatBytes, a.ws.nlse2 + g * kTile, kTile * 4, qb);
           bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.ndsum + g * kTile, kTile * 4, qb);
           q_issued = q_it + 1;
+          ATTN_TRACE_EV(43, q_it);
           if (!(ok = mbar_wait(smem_u32(&bars->do_empty[st]), par, ab))) break;
           ATTN_TRACE_EV(41, q_it);
           const uint32_t db = smem_u32(&bars->do_full[st]);
           mbar_arrive_expect_tx(db, C::kdOBytes);
           for (int p = 0; p < C::kVPanels; ++p)
             tma_load_3d(sdO_of(st) + p * kPanelBytes, &tm_do, db, p * 64, it.head, qrow);
+          do_issued = q_it + 1;
+          ATTN_TRACE_EV(42, q_it);
         }
         if (!ok) break;
       }
@@ -485,7 +529,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (kv_issued) mbar_wait_drain(smem_u32(&bars->kv_full), kq & 1);
         for (uint32_t t = q_issued > (uint32_t)C::kStages ? q_issued - C::kStages : 0; t < q_issued; ++t)
           mbar_wait_drain(smem_u32(&bars->q_full[t % C::kStages]), (t / C::kStages) & 1);
-        for (uint32_t t = q_it > (uint32_t)C::kStages ? q_it - C::kStages : 0; t < q_it; ++t)
+        for (uint32_t t = do_issued > (uint32_t)C::kStages ? do_issued - C::kStages : 0; t < do_issued; ++t)
           mbar_wait_drain(smem_u32(&bars->do_full[t % C::kStages]), (t / C::kStages) & 1);
       }
     }
@@ -665,6 +709,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
     }
    }
+#ifdef ATTN_TRACE
+   else if ((warp == 14 || warp == 15) && lane == 0 && a.trace != nullptr && blockIdx.x == 0) {
+    // trace builds only: record when the traced steps' dO (warp 14) and Q
+    // (warp 15) stages land
+    uint64_t* full = warp == 14 ? bars->do_full : bars->q_full;
+    for (uint32_t t = 0; t < kTraceFrom + kTraceSteps; ++t) {
+      if (!mbar_wait(smem_u32(&full[t % C::kStages]), (t / C::kStages) & 1, ab)) break;
+      ATTN_TRACE_EV(warp == 14 ? 44 : 45, t);
+    }
+   }
+#endif
   } else if (warp < 8) {
     regs_dec<RegSplit<DQK>::kCompute>();
     // ================================================= P / dS warpgroups
@@ -793,6 +848,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int wt = threadIdx.x - 8 * 32;  // 0..127 within this warpgroup
     uint32_t gi = 0;
     bool ok = true;
+    // Pacing of the dQ reductions.  Issued back to back, the 128 threads'
+    // DQK/4 vector reductions fill the SM's queue to the L2 faster than it
+    // drains (32 bytes per clock), and every shared-memory access and
+    // barrier wait of the other roles queues behind them — the MMA issuer's
+    // waits and the dS stores stall for about a thousand cycles per q-tile.
+    // Spreading the reductions over about 70 % of the q-tile step (measured
+    // between consecutive dQ tiles, capped) keeps the queue short.
+    // In deterministic mode the next kv tile's contribution waits for this
+    // one's reductions, so they go out unpaced.
+    long long t_prev = 0;
+    int pace = a.deterministic ? 0 : kRedPaceCap;
     for (uint32_t k = 0; ok; ++k) {
       const uint32_t slot = k & 1;
       if (!(ok = mbar_wait_warp(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
@@ -824,6 +890,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (a.deterministic && wt == 0) target_m = wait_target();
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
+        {
+          const long long t_now = clock64();
+          if (t_prev != 0) {
+            const long long step = t_now - t_prev;
+            pace = a.deterministic ? 0
+                   : kRedSpread > 0
+                       ? (int)min((long long)kRedPaceCap, step * kRedSpread / (256 * (DQK / 4)))
+                       : kRedPaceCap;
+          }
+          t_prev = t_now;
+        }
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(30, gi);
         uint32_t qv[DQK];
 #pragma unroll
@@ -854,11 +931,24 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           named_bar_sync(1, 128);
           if (ab.raised()) { ok = false; break; }
         }
+        if (pace > 0) {
+          const long long t0 = clock64();
 #pragma unroll
-        for (int c4 = 0; c4 < DQK / 4; ++c4)
-          red_add_v4(acc + (c4 * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
-                     __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
-                     __uint_as_float(qv[c4 * 4 + 3]));
+          for (int c4 = 0; c4 < DQK / 4; ++c4) {
+            red_add_v4(acc + (c4 * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+                       __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
+                       __uint_as_float(qv[c4 * 4 + 3]));
+            const long long due = t0 + (long long)(c4 + 1) * pace;
+            while (clock64() < due) {
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < DQK / 4; ++c4)
+            red_add_v4(acc + (c4 * kTile + r) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+                       __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
+                       __uint_as_float(qv[c4 * 4 + 3]));
+        }
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(32, gi);
         if (a.deterministic) {
           named_bar_sync(1, 128);
@@ -1025,12 +1115,13 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     } else {
       auto* k = L.sh.blk != nullptr ? attn_bwd_main_kernel<DQK, DV, Tables, true>
                                     : attn_bwd_main_kernel<DQK, DV, Tables, false>;
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmemBytes + kTraceSmem);
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(L.grid);
       cfg.blockDim = dim3(kMainThreads);
-      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.dynamicSmemBytes = C::kSmemBytes + kTraceSmem;
       cfg.stream = L.stream;
       e = cudaLaunchKernelEx(&cfg, k, L.tm_q, L.tm_k, L.tm_v, L.tm_do, a, tb);
     }

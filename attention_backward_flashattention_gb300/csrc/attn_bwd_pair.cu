@@ -624,6 +624,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int wt = threadIdx.x - 8 * 32;
     uint32_t gi = 0;
     bool ok = !misaligned;
+    // the reductions are paced as in the one-CTA kernel (fast mode only)
+    long long t_prev = 0;
+    int pace = a.deterministic ? 0 : kRedPaceCap;
     for (uint32_t k = 0; ok; ++k) {
       const uint32_t slot = k & 1;
       if (!(ok = mbar_wait_cluster_warp(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
@@ -639,6 +642,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dq_full), gi & 1, ab))) break;
         tc_fence_after();
         if (lane == 0 && warp == 8) PAIR_TRACE(30, gi);
+        {
+          const long long t_now = clock64();
+          if (t_prev != 0 && !a.deterministic)
+            pace = (int)min((long long)kRedPaceCap, (t_now - t_prev) * kRedSpread / (256 * 16));
+          t_prev = t_now;
+        }
         uint32_t qv[64];
         tmem_ld32(tmem + lane_base + C::kTmemdQ, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
         tmem_ld32(tmem + lane_base + C::kTmemdQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
@@ -668,11 +677,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           named_bar_sync(1, 128);
           if (ab.raised()) { ok = false; break; }
         }
+        if (pace > 0) {
+          const long long t0 = clock64();
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4)
-          red_add_v4(acc + ((dh * 16 + c4) * kTile + qr) * 4, __uint_as_float(qv[c4 * 4 + 0]),
-                     __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
-                     __uint_as_float(qv[c4 * 4 + 3]));
+          for (int c4 = 0; c4 < 16; ++c4) {
+            red_add_v4(acc + ((dh * 16 + c4) * kTile + qr) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+                       __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
+                       __uint_as_float(qv[c4 * 4 + 3]));
+            const long long due = t0 + (long long)(c4 + 1) * pace;
+            while (clock64() < due) {
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4)
+            red_add_v4(acc + ((dh * 16 + c4) * kTile + qr) * 4, __uint_as_float(qv[c4 * 4 + 0]),
+                       __uint_as_float(qv[c4 * 4 + 1]), __uint_as_float(qv[c4 * 4 + 2]),
+                       __uint_as_float(qv[c4 * 4 + 3]));
+        }
         if (lane == 0 && warp == 8) PAIR_TRACE(32, gi);
         if (a.deterministic) {
           named_bar_sync(1, 128);

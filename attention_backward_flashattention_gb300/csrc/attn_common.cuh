@@ -40,6 +40,12 @@ namespace attn {
 constexpr int kTile = 128;
 constexpr int kFwdRows = 2 * kTile;  // query rows of one forward work item (two Q tiles)
 constexpr int kMaxSeqs = 1024;  // sequences in one variable-length call
+// Pacing of the backward's fp32 dQ reductions (fast mode): one thread's
+// reductions of a dQ tile are spread over kRedSpread/256 of the previous
+// q-tile step (the time between the two previous dQ tiles), with at most
+// kRedPaceCap clocks between two of them.
+constexpr int kRedPaceCap = 128;
+constexpr long long kRedSpread = 179;
 
 // Host-computed tables for variable-length batches (passed by value).
 struct VarlenTables {
