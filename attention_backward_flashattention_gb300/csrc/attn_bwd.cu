@@ -499,28 +499,43 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const uint32_t par = ((q_it / C::kStages) & 1) ^ 1;
           const int qrow = it.row0 + i * kTile;
           const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
-          if (!(ok = mbar_wait(smem_u32(&bars->q_empty[st]), par, ab))) break;
-          ATTN_TRACE_EV(40, q_it);
-          // under a block mask the MMA issuer learns from this flag whether
-          // another q-tile follows (published by the arrive below, read after
-          // its wait on q_full)
-          if constexpr (kMask) bars->q_last[st] = inext >= i1 ? 1 : 0;
-          const uint32_t qb = smem_u32(&bars->q_full[st]);
-          mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
-          for (int p = 0; p < C::kQPanels; ++p)
-            tma_load_3d(sQ_of(st) + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
-          bulk_load(sStat + st * C::kStatBytes, a.ws.nlse2 + g * kTile, kTile * 4, qb);
-          bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.ndsum + g * kTile, kTile * 4, qb);
-          q_issued = q_it + 1;
-          ATTN_TRACE_EV(43, q_it);
-          if (!(ok = mbar_wait(smem_u32(&bars->do_empty[st]), par, ab))) break;
-          ATTN_TRACE_EV(41, q_it);
-          const uint32_t db = smem_u32(&bars->do_full[st]);
-          mbar_arrive_expect_tx(db, C::kdOBytes);
-          for (int p = 0; p < C::kVPanels; ++p)
-            tma_load_3d(sdO_of(st) + p * kPanelBytes, &tm_do, db, p * 64, it.head, qrow);
-          do_issued = q_it + 1;
-          ATTN_TRACE_EV(42, q_it);
+          // Q (with the row statistics) and dO of the q-tile.  dO's stage is
+          // released by dV, early in a step, and Q's by dK, late in it: at
+          // d <= 128 dO goes first, so that it lands a step ahead of dP; at
+          // d = 192 (S and dP share their columns) Q first measured faster.
+          auto load_q = [&]() -> bool {
+            if (!mbar_wait(smem_u32(&bars->q_empty[st]), par, ab)) return false;
+            ATTN_TRACE_EV(40, q_it);
+            // under a block mask the MMA issuer learns from this flag whether
+            // another q-tile follows (published by the arrive below, read
+            // after its wait on q_full)
+            if constexpr (kMask) bars->q_last[st] = inext >= i1 ? 1 : 0;
+            const uint32_t qb = smem_u32(&bars->q_full[st]);
+            mbar_arrive_expect_tx(qb, C::kQBytes + C::kStatBytes);
+            for (int p = 0; p < C::kQPanels; ++p)
+              tma_load_3d(sQ_of(st) + p * kPanelBytes, &tm_q, qb, p * 64, it.head, qrow);
+            bulk_load(sStat + st * C::kStatBytes, a.ws.nlse2 + g * kTile, kTile * 4, qb);
+            bulk_load(sStat + st * C::kStatBytes + kTile * 4, a.ws.ndsum + g * kTile, kTile * 4, qb);
+            q_issued = q_it + 1;
+            ATTN_TRACE_EV(43, q_it);
+            return true;
+          };
+          auto load_do = [&]() -> bool {
+            if (!mbar_wait(smem_u32(&bars->do_empty[st]), par, ab)) return false;
+            ATTN_TRACE_EV(41, q_it);
+            const uint32_t db = smem_u32(&bars->do_full[st]);
+            mbar_arrive_expect_tx(db, C::kdOBytes);
+            for (int p = 0; p < C::kVPanels; ++p)
+              tma_load_3d(sdO_of(st) + p * kPanelBytes, &tm_do, db, p * 64, it.head, qrow);
+            do_issued = q_it + 1;
+            ATTN_TRACE_EV(42, q_it);
+            return true;
+          };
+          if constexpr (C::kSharedSdP) {
+            if (!(ok = load_q() && load_do())) break;
+          } else {
+            if (!(ok = load_do() && load_q())) break;
+          }
         }
         if (!ok) break;
       }
@@ -853,7 +868,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // drains (32 bytes per clock), and every shared-memory access and
     // barrier wait of the other roles queues behind them — the MMA issuer's
     // waits and the dS stores stall for about a thousand cycles per q-tile.
-    // Spreading the reductions over about 70 % of the q-tile step (measured
+    // Spreading the reductions over about 80 % of the q-tile step (measured
     // between consecutive dQ tiles, capped) keeps the queue short.
     // In deterministic mode the next kv tile's contribution waits for this
     // one's reductions, so they go out unpaced.

@@ -45,7 +45,7 @@ constexpr int kMaxSeqs = 1024;  // sequences in one variable-length call
 // q-tile step (the time between the two previous dQ tiles), with at most
 // kRedPaceCap clocks between two of them.
 constexpr int kRedPaceCap = 128;
-constexpr long long kRedSpread = 179;
+constexpr long long kRedSpread = 205;
 
 // Host-computed tables for variable-length batches (passed by value).
 struct VarlenTables {
