@@ -333,6 +333,42 @@ struct BwdCfg {
   static_assert(kTmemdQ + DQK <= kTmemCols, "tensor memory budget (dQ)");
 };
 
+// Epilogue helpers: N accumulator columns of this thread's TMEM lane, scaled,
+// as bf16 pairs (zeros when nothing was accumulated), and their store as one
+// row of the caller's layout (32-byte stores when st32).
+template <int N>
+__device__ __forceinline__ void epi_read(uint32_t taddr, float sc, bool zero,
+                                         uint32_t (&pk)[N / 2]) {
+  if (zero) {
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) pk[e] = 0u;
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < N / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pk[c * 16 + e] = pack_bf16(__uint_as_float(v[2 * e]) * sc, __uint_as_float(v[2 * e + 1]) * sc);
+  }
+}
+template <int N>
+__device__ __forceinline__ void epi_store(__nv_bfloat16* dst, int st32, const uint32_t (&pk)[N / 2]) {
+  if (st32) {
+#pragma unroll
+    for (int j = 0; j < N / 16; ++j)
+      st_global_v8(dst + j * 16, pk[8 * j + 0], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3],
+                   pk[8 * j + 4], pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j)
+      *reinterpret_cast<uint4*>(dst + j * 8) =
+          make_uint4(pk[4 * j + 0], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  }
+}
+
 // TMEM column of the packed P^T operand for MMA K-step kk (16 queries).
 __device__ __forceinline__ uint32_t p_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
@@ -358,7 +394,8 @@ constexpr int kMaxStages = 4;
 
 struct BwdBars {
   uint64_t item_full[2], item_empty[2];
-  uint64_t kv_full, kv_done, acc_free;
+  uint64_t kv_full, kv_done;
+  uint64_t accv_free, acck_free;  // the epilogue has read the dV / dK accumulator
   uint64_t q_full[kMaxStages], q_empty[kMaxStages];    // Q panels + LSE2 + D of a q-tile
   uint64_t do_full[kMaxStages], do_empty[kMaxStages];  // dO panels
   uint64_t s_full, p_full, dp_full, dq_full, dq_free;
@@ -374,6 +411,7 @@ static_assert(sizeof(BwdBars) <= 512, "barrier block size");
 
 struct MainArgs {
   int sem_bias;  // 0; a test sets it so that the ordered dQ wait can never succeed
+  int st32;      // dK and dV rows are 32-byte aligned: 32-byte stores
 #ifdef ATTN_TRACE
   unsigned long long* trace;  // kMainThreads x kTraceCap records
 #endif
@@ -428,7 +466,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_done), 1);
-    mbar_init(smem_u32(&bars->acc_free), 4);
+    mbar_init(smem_u32(&bars->accv_free), 4);
+    mbar_init(smem_u32(&bars->acck_free), 4);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bars->q_full[s]), 1);
       mbar_init(smem_u32(&bars->q_empty[s]), 1);
@@ -629,7 +668,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!(ok = W(bars->kv_full, k & 1))) break;
         if (none) {
           // dK/dV accumulators of the previous item read out by the epilogue
-          if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+          if (!(ok = W(bars->accv_free, (k & 1) ^ 1) && W(bars->acck_free, (k & 1) ^ 1))) break;
         }
         if (none) {
           // no query sees this kv tile (a local window or a block mask): the
@@ -646,8 +685,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_dP(st0);
           // the previous item's dK/dV accumulators must be read out by its
           // epilogue before this item's first dV; waiting here, after the first
-          // S and dP, lets the epilogue overlap them
-          if (!(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+          // S and dP, lets the epilogue overlap them (at d <= 128 the epilogue
+          // releases both accumulators at once)
+          if (!(ok = W(bars->accv_free, (k & 1) ^ 1))) break;
           bool go = true;  // kMask: the previous q-tile was not the item's last
           for (int i = i0; kMask ? go : i < i1; ++i, ++q_it, ++gi) {
             const uint32_t st = q_it % C::kStages;
@@ -701,7 +741,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             if (!(ok = W(bars->do_full[st], par))) break;
             // the previous item's dK/dV accumulators read out by its epilogue,
             // which overlaps this item's first S and P
-            if (first && !(ok = W(bars->acc_free, (k & 1) ^ 1))) break;
+            if (first && !(ok = W(bars->accv_free, (k & 1) ^ 1) && W(bars->acck_free, (k & 1) ^ 1)))
+              break;
             mma_dV(st, first);
             mma_dP(st);  // overwrites the S/P columns after dV has read P
             mma_commit(smem_u32(&bars->do_empty[st]));
@@ -980,54 +1021,54 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const int kidx = it.tile * kTile + r;
       const bool key_ok = kidx < it.Lk;
       const int krow = key_row0(sh, it) + kidx;
-#pragma unroll 1
-      for (int c = 0; c < DQK / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kTmemdK + c * 32, v);
-        tmem_ld_wait();
-        if (ifirst >= i1) {  // no query sees this kv tile: nothing was accumulated
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
+      const bool nothing = ifirst >= i1;  // no query sees this kv tile: zeros
+      auto dk_row = [&]() { return a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK; };
+      auto dv_row = [&]() { return a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV; };
+      if constexpr (C::kSharedSdP) {
+        // d = 192: each accumulator is read whole into bf16 pairs and released
+        // before its row is stored (32-byte stores when aligned), so that the
+        // next item's first dV and dK need not wait for the stores
+        {
+          uint32_t pk[DV / 2];
+          epi_read<DV>(tmem + lane_base + C::kTmemdV, 1.0f, nothing, pk);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->accv_free));
+          if (key_ok) epi_store<DV>(dv_row(), a.st32, pk);
         }
-        if (key_ok) {
-          __nv_bfloat16* dst = a.dk + (int64_t)krow * a.dk_row_stride + (int64_t)it.head * DQK + c * 32;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * a.scale, __uint_as_float(v[q4 * 8 + 1]) * a.scale);
-            w.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * a.scale, __uint_as_float(v[q4 * 8 + 3]) * a.scale);
-            w.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * a.scale, __uint_as_float(v[q4 * 8 + 5]) * a.scale);
-            w.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * a.scale, __uint_as_float(v[q4 * 8 + 7]) * a.scale);
-            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
-          }
+        {
+          uint32_t pk[DQK / 2];
+          epi_read<DQK>(tmem + lane_base + C::kTmemdK, a.scale, nothing, pk);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->acck_free));
+          if (key_ok) epi_store<DQK>(dk_row(), a.st32, pk);
+        }
+      } else {
+        // d <= 128: 32 columns at a time, each read followed by its stores
+        // (spacing the stores out), both accumulators released at the end —
+        // this measured faster here than releasing them early
+#pragma unroll 1
+        for (int c = 0; c < DQK / 32; ++c) {
+          uint32_t pk[16];
+          epi_read<32>(tmem + lane_base + C::kTmemdK + c * 32, a.scale, nothing, pk);
+          if (key_ok) epi_store<32>(dk_row() + c * 32, 0, pk);
+        }
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t pk[16];
+          epi_read<32>(tmem + lane_base + C::kTmemdV + c * 32, 1.0f, nothing, pk);
+          if (key_ok) epi_store<32>(dv_row() + c * 32, 0, pk);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->accv_free));
+          mbar_arrive(smem_u32(&bars->acck_free));
         }
       }
-#pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kTmemdV + c * 32, v);
-        tmem_ld_wait();
-        if (ifirst >= i1) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
-        }
-        if (key_ok) {
-          __nv_bfloat16* dst = a.dv + (int64_t)krow * a.dv_row_stride + (int64_t)it.head * DV + c * 32;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]), __uint_as_float(v[q4 * 8 + 1]));
-            w.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]), __uint_as_float(v[q4 * 8 + 3]));
-            w.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]), __uint_as_float(v[q4 * 8 + 5]));
-            w.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]), __uint_as_float(v[q4 * 8 + 7]));
-            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
-          }
-        }
-      }
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->acc_free));
         mbar_arrive(smem_u32(&bars->item_empty[slot]));
       }
     }
@@ -1118,6 +1159,8 @@ cudaError_t launch_all(const BwdLaunch& L, const Tables& tb) {
     a.scale_log2 = L.scale_log2;
     a.deterministic = L.deterministic;
     a.sem_bias = L.sem_bias;
+    a.st32 = ((reinterpret_cast<uintptr_t>(L.dk) | reinterpret_cast<uintptr_t>(L.dv)) & 31u) == 0 &&
+             (L.dk_row_stride * 2) % 32 == 0 && (L.dv_row_stride * 2) % 32 == 0;
 #ifdef ATTN_TRACE
     a.trace = g_trace_buf;
 #endif
