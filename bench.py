@@ -313,36 +313,68 @@ def _time_loop(stream, steps, body):
 
 def e2e_step_host(args, w, x, dev, stream, K):
     """Host tensors in, gradients out, through attn_step_host (fixed-length
-    (B,T,H,d) only): ms per step and the bytes copied each way."""
+    (B,T,H,d) only): ms per step and the bytes copied each way.
+
+    With --e2e-slots 2 (the default) consecutive steps alternate between two
+    scratch buffers, each with its own streams and host output tensors, the
+    way a training loop double-buffers its batches: step k+1's input copies
+    run while step k's kernels and gradient copies finish.  Every step still
+    copies all its inputs in and all its gradients out inside the timed
+    region."""
     B, H, T, dqk, dv = w.B, w.H, w.T, w.dqk, w.dv
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dO"))
-    hdq, hdk, hdv = (torch.empty(x[n].shape, dtype=torch.bfloat16, pin_memory=True)
-                     for n in ("q", "k", "v"))
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
     G = args.e2e_heads_per_group
     scratch_bytes = binding.attn_step_host_scratch_size(B, H, T, dqk, dv, G, w.deterministic)
-    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=dev)
-    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    stream2 = torch.cuda.Stream(dev) if args.e2e_streams == 2 else None
+    slots = []
+    for i in range(max(1, args.e2e_slots)):
+        slots.append({
+            "out": tuple(torch.empty(x[n].shape, dtype=torch.bfloat16, pin_memory=True)
+                         for n in ("q", "k", "v")),
+            "scratch": torch.empty(scratch_bytes, dtype=torch.uint8, device=dev),
+            "cs": stream if i == 0 else torch.cuda.Stream(dev),
+            "cs2": torch.cuda.Stream(dev) if args.e2e_streams == 2 else None,
+            "hs": torch.cuda.Stream(dev), "ds": torch.cuda.Stream(dev)})
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in slots[0]["out"])
 
-    def step():
+    def step(k):
+        sl = slots[k % len(slots)]
+        hdq, hdk, hdv = sl["out"]
         rc = binding.attn_step_host(hq, hk, hv, hdo, None, hdq, hdk, hdv, B, H, T, dqk, dv,
-                                    w.causal, w.scale, w.deterministic, G, scratch,
-                                    scratch_bytes, stream, stream2, h2d_stream, d2h_stream)
+                                    w.causal, w.scale, w.deterministic, G, sl["scratch"],
+                                    scratch_bytes, sl["cs"], sl["cs2"], sl["hs"], sl["ds"])
         assert rc == 0, rc
 
-    step()
+    def status_ok():
+        return all(binding.attn_step_host_status(sl["scratch"], B, H, T, dqk, dv, G,
+                                                 w.deterministic, sl["cs"]) == 0 for sl in slots)
+
+    for k in range(len(slots)):
+        step(k)
     torch.cuda.synchronize()
-    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+    if not status_ok():
         raise RuntimeError("device status error in the e2e warm-up")
-    ms = _time_loop(stream, K, step) / K
-    if binding.attn_step_host_status(scratch, B, H, T, dqk, dv, G, w.deterministic, stream):
+    a, b = _events(2)
+    a.record(stream)
+    for sl in slots[1:]:
+        sl["cs"].wait_event(a)
+    for k in range(K):
+        step(k)
+    for sl in slots[1:]:
+        e = torch.cuda.Event()
+        e.record(sl["cs"])
+        stream.wait_event(e)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    if not status_ok():
         raise RuntimeError("device status error in the e2e region")
     api = ("attn_step_host (pinned host tensors; forward + backward; copies of one head group "
-           "overlap the kernels of another)")
+           "overlap the kernels of another"
+           + ("; consecutive steps alternate between %d scratch buffers, so one step's copies "
+              "overlap the next step's kernels" % len(slots) if len(slots) > 1 else "") + ")")
     return ms, h2d, d2h, api, {"heads_per_group": G or -(-H // 2),
-                               "compute_streams": args.e2e_streams}
+                               "compute_streams": args.e2e_streams, "slots": len(slots)}
 
 
 def e2e_copies(w, x, prob, stream, K):
@@ -739,6 +771,8 @@ def main():
                     help="head-group size of the e2e pipeline (0: the library's choice)")
     ap.add_argument("--e2e-streams", type=int, default=1, choices=(1, 2),
                     help="compute streams of the e2e pipeline")
+    ap.add_argument("--e2e-slots", type=int, default=2, choices=(1, 2),
+                    help="scratch buffers that consecutive e2e steps alternate between")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the inference-mode forward (lse=NULL) instead of the step")
     ap.add_argument("--block-density", type=float, default=0.0,
