@@ -400,7 +400,6 @@ struct BwdBars {
   uint64_t do_full[kMaxStages], do_empty[kMaxStages];  // dO panels
   uint64_t s_full, p_full, dp_full, dq_full, dq_free;
   uint64_t ds_half[2];  // dS^T columns 0-31 / 64-95 (half 0) and 32-63 / 96-127 (half 1)
-  uint64_t ds_free;     // the dK and dQ products are done reading dS^T
   uint64_t drain;
   int item_slot[2];
   int q_last[kMaxStages];  // 1: the stage's q-tile is its item's last (written with q_full)
@@ -480,7 +479,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(smem_u32(&bars->ds_half[0]), 8);
     mbar_init(smem_u32(&bars->ds_half[1]), 8);
     mbar_init(smem_u32(&bars->dq_full), 1);
-    mbar_init(smem_u32(&bars->ds_free), 1);
     mbar_init(smem_u32(&bars->dq_free), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
@@ -717,7 +715,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             ATTN_TRACE_EV(16, gi);
             mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
-            mma_commit(smem_u32(&bars->ds_free));
             if (more) {
               if (C::kDqOnDp && !(ok = W(bars->dq_free, gi & 1))) break;
               ATTN_TRACE_EV(13, gi);
@@ -752,7 +749,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mma_dK(st, first, 1);
             mma_commit(smem_u32(&bars->q_empty[st]));
             mma_dQ();
-            mma_commit(smem_u32(&bars->ds_free));
           }
         }
         if (!ok) break;
@@ -857,8 +853,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!(ok = mbar_wait_warp(smem_u32(&bars->dp_full), gi & 1, ab))) break;
         tc_fence_after();
         if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(22, gi);
-        // the previous dS tile must have been consumed by its dK and dQ products
-        if (gi > 0 && !(ok = mbar_wait_warp(smem_u32(&bars->ds_free), (gi - 1) & 1, ab))) break;
+        // The previous dS tile has been consumed: its dK and dQ products were
+        // issued before this dP, and the commit behind dp_full tracks every
+        // product issued before it, so no separate wait is needed here.
         if (lane == 0 && (warp & 3) == 0) ATTN_TRACE_EV(25, gi);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
