@@ -1043,19 +1043,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
       } else {
         // d <= 128: 32 columns at a time, each read followed by its stores
-        // (spacing the stores out), both accumulators released at the end —
-        // this measured faster here than releasing them early
+        // (spacing the stores out; 32-byte stores when aligned), both
+        // accumulators released at the end — this measured faster here than
+        // releasing them early
 #pragma unroll 1
         for (int c = 0; c < DQK / 32; ++c) {
           uint32_t pk[16];
           epi_read<32>(tmem + lane_base + C::kTmemdK + c * 32, a.scale, nothing, pk);
-          if (key_ok) epi_store<32>(dk_row() + c * 32, 0, pk);
+          if (key_ok) epi_store<32>(dk_row() + c * 32, a.st32, pk);
         }
 #pragma unroll 1
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t pk[16];
           epi_read<32>(tmem + lane_base + C::kTmemdV + c * 32, 1.0f, nothing, pk);
-          if (key_ok) epi_store<32>(dv_row() + c * 32, 0, pk);
+          if (key_ok) epi_store<32>(dv_row() + c * 32, a.st32, pk);
         }
         tc_fence_before();
         __syncwarp();

@@ -339,3 +339,29 @@ def test_running_max_jumps_between_key_tiles(causal):
     x["k"] = k.bfloat16()
     g = gc.run_gpu(x, w)
     gc.assert_within(gc.compare_full(x, w, g), f"jump causal={causal}")
+
+
+@pytest.mark.parametrize("dqk,dv", [(128, 128), (192, 128)])
+def test_gradient_buffers_only_16_byte_aligned(dqk, dv):
+    """dK and dV rows are written with 32-byte stores when the buffers allow it
+    and with 16-byte stores otherwise; both give the same bits (deterministic
+    mode), and dQ is unaffected."""
+    B, H, T = 1, 2, 300
+    w = syn.Workload("align16", B=B, H=H, T=T, dqk=dqk, dv=dv, causal=True)
+    x = syn.make_inputs(w, seed=21)
+    dev = "cuda:0"
+    q, k, v, dO = (x[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
+    ref = binding.backward(q, k, v, o, dO, lse, causal=True, scale=w.scale, deterministic=True)
+
+    def shifted(t):  # same shape, data starting 16 bytes past a 256-byte boundary
+        buf = torch.empty(t.numel() + 8, dtype=torch.bfloat16, device=dev)
+        return buf[8:].view(t.shape)
+
+    out = (shifted(q), shifted(k), shifted(v))
+    assert all(t.data_ptr() % 32 == 16 for t in out)
+    got = binding.backward(q, k, v, o, dO, lse, causal=True, scale=w.scale, deterministic=True,
+                           out=out)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
