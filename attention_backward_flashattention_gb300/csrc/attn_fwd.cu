@@ -679,20 +679,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const bool no_key = kMask && !(l > 0.f);
       const float inv_l = no_key ? 0.f : 1.0f / l;
+      // O rows 32-byte aligned (base and row stride)
+      const bool st32 = ((reinterpret_cast<uintptr_t>(out) | (uintptr_t)(o_row_stride * 2)) & 31u) == 0;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait();
         if (valid) {
+          uint32_t pw[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(ov[q4 * 8 + 0]) * inv_l, __uint_as_float(ov[q4 * 8 + 1]) * inv_l);
-            v.y = pack_bf16(__uint_as_float(ov[q4 * 8 + 2]) * inv_l, __uint_as_float(ov[q4 * 8 + 3]) * inv_l);
-            v.z = pack_bf16(__uint_as_float(ov[q4 * 8 + 4]) * inv_l, __uint_as_float(ov[q4 * 8 + 5]) * inv_l);
-            v.w = pack_bf16(__uint_as_float(ov[q4 * 8 + 6]) * inv_l, __uint_as_float(ov[q4 * 8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = v;
+          for (int e = 0; e < 16; ++e)
+            pw[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+          if (st32) {  // 32-byte stores: half the requests of 16-byte ones
+            st_global_v8(orow + c * 32, pw[0], pw[1], pw[2], pw[3], pw[4], pw[5], pw[6], pw[7]);
+            st_global_v8(orow + c * 32 + 16, pw[8], pw[9], pw[10], pw[11], pw[12], pw[13], pw[14],
+                         pw[15]);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) =
+                  make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
           }
         }
       }

@@ -365,3 +365,23 @@ def test_gradient_buffers_only_16_byte_aligned(dqk, dv):
     torch.cuda.synchronize()
     for a, b in zip(got, ref):
         assert torch.equal(a, b)
+
+
+def test_forward_output_only_16_byte_aligned():
+    """O rows are written with 32-byte stores when the buffer allows it and
+    with 16-byte stores otherwise; both give the same bits."""
+    B, H, T, d = 1, 2, 300, 128
+    w = syn.Workload("align16_fwd", B=B, H=H, T=T, dqk=d, dv=d, causal=True)
+    x = syn.make_inputs(w, seed=22)
+    dev = "cuda:0"
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o_ref, lse_ref = binding.forward(q, k, v, causal=True, scale=w.scale)
+    buf = torch.empty(o_ref.numel() + 8, dtype=torch.bfloat16, device=dev)
+    o = buf[8:].view(o_ref.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty_like(lse_ref)
+    rc = binding.attn_fwd_ex(q, k, v, o, lse, B, H, T, T, d, d, True, -1, -1, None, 1, 1,
+                             w.scale, None, None, binding.LAYOUT_BTHD, None)
+    assert rc == binding.ATTN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
