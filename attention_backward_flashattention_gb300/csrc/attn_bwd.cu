@@ -912,6 +912,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // one's reductions, so they go out unpaced.
     long long t_prev = 0;
     int pace = a.deterministic ? 0 : kRedPaceCap;
+    // Deterministic mode at d <= 128: the "added" mark of a q-tile is released
+    // after the NEXT q-tile's drain, so that the fence it needs (the
+    // reductions must reach the L2 first) does not hold up that drain — the
+    // kv tile below, which reaches this q-tile about one step later, finds it
+    // by then.  At d = 192 (no registers to spare) it goes out at once.
+    constexpr bool kDeferRelease = !C::kSharedSdP;
+    int64_t rel_word = -1;
+    int rel_val = 0;
     for (uint32_t k = 0; ok; ++k) {
       const uint32_t slot = k & 1;
       if (!(ok = mbar_wait_warp(smem_u32(&bars->item_full[slot]), (k >> 1) & 1, ab))) break;
@@ -965,6 +973,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(31, gi);
+        if (kDeferRelease && wt == 0 && rel_word >= 0) {  // the previous q-tile's mark
+          __threadfence();
+          st_release_gpu(a.ws.sem + rel_word, rel_val);
+          rel_word = -1;
+        }
         const int64_t g = (int64_t)(it.tile_base + i) * sh.H + it.head;
         float* acc = a.ws.dq_acc + g * (kTile * DQK);
         if (a.deterministic) {
@@ -1004,12 +1017,23 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
         if (lane == 0 && warp == 8) ATTN_TRACE_EV(32, gi);
         if (a.deterministic) {
-          named_bar_sync(1, 128);
+          named_bar_sync(1, 128);  // every thread's reductions issued
           if (wt == 0) {
-            __threadfence();
-            st_release_gpu(a.ws.sem + 2 * g, it.tile + 1);
+            if constexpr (kDeferRelease) {
+              rel_word = 2 * g;
+              rel_val = it.tile + 1;
+            } else {
+              __threadfence();
+              st_release_gpu(a.ws.sem + 2 * g, it.tile + 1);
+            }
           }
         }
+      }
+      // the item's last mark goes out before the epilogue
+      if (kDeferRelease && wt == 0 && rel_word >= 0) {
+        __threadfence();
+        st_release_gpu(a.ws.sem + rel_word, rel_val);
+        rel_word = -1;
       }
       if (!ok) break;
       // ---- epilogue: dK = s * acc, dV = acc (thread = key row r)
